@@ -1,0 +1,384 @@
+#!/usr/bin/env python3
+"""Throughput of the chunked gated delta rule forward on GB300.
+
+One step = one whole forward (chunk enumeration, prep, state scan, output) over
+the packed 64k-token workload: 65536 tokens in segments of uniform random
+length in [1, 8192] plus 16 trailing length-0 segments, H = 32 heads,
+dk = dv = 128, bf16 q/k/v/beta, fp32 g, no initial or final state.  Inputs are
+seeded synthetic tensors (q, k L2-normalised, v Gaussian, g = logsigmoid(N(3,1)),
+beta = sigmoid(N(0,1))) resident in HBM before timing; they total 2.16 GB, more
+than the 129 MB L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
+on the host cores instead (a deliberately slow baseline).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDR chunk-fwd tokens/s (H=32, d=128, 64k packed) & % of tensor/HBM roofline"
+WORKLOAD = "packed_64k_h32"
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gdr_fused_fwd_packed_64k_h32.md")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--path", choices=["auto", "fused", "staged"], default="auto")
+    p.add_argument("--workload", default=WORKLOAD)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="target CPU seconds for the oracle sample")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def algorithmic_bytes(w) -> int:
+    """q, k, v, o in bf16; g in fp32; beta in bf16; h0/ht in fp32 when present."""
+    T, Hk, H, dk, dv = w.T, w.Hk, w.H, w.dk, w.dv
+    b = T * (2 * dk * Hk * 2 + 2 * dv * H * 2 + 4 * H + 2 * H)
+    state = w.n_seq * H * dk * dv * 4
+    b += state * ((w.h0 is not None) + bool(w.want_ht))
+    return int(b)
+
+
+def algorithmic_flops(w) -> int:
+    """Dense-tile FLOPs, 2 (5 c^2 d + 3 c d^2) per chunk of c tokens per value head."""
+    d = w.dk
+    f = 0
+    for n in w.lengths():
+        full, rem = divmod(n, 64)
+        f += full * 2 * (5 * 64 * 64 * d + 3 * 64 * d * d)
+        if rem:
+            f += 2 * (5 * rem * rem * d + 3 * rem * d * d)
+    return int(f * w.H)
+
+
+def read_traffic(expected_sha: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (same sha256), else None."""
+    try:
+        txt = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    sha = traffic = None
+    for line in txt.splitlines():
+        if line.startswith("source_sha256:"):
+            sha = line.split(":", 1)[1].strip()
+        if line.startswith("dram_bytes_per_launch:"):
+            try:
+                traffic = float(line.split(":", 1)[1].strip())
+            except ValueError:
+                traffic = None
+    return traffic if (sha and sha == expected_sha) else None
+
+
+def kernel_sha() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "chunked_gated_delta_gdr_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"gdr_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_oracle_sample(w, target_s: float):
+    """Time the fp64 oracle on a head subset of the workload sized to ~target_s."""
+    import oracle
+    from chunked_gated_delta_gdr_gb300.inputs import Workload  # noqa: F401
+    threads = oracle.max_threads()
+
+    def run(heads):
+        sel = lambda t: t[:, heads].contiguous()
+        hk = [h // (w.H // w.Hk) for h in heads]
+        t0 = time.perf_counter()
+        oracle.recurrent(w.q[:, hk].contiguous(), w.k[:, hk].contiguous(), sel(w.v),
+                         sel(w.g), sel(w.beta), w.scale,
+                         None if w.h0 is None else w.h0[:, heads].contiguous(),
+                         w.cu_seqlens, want_ht=w.want_ht)
+        return time.perf_counter() - t0
+
+    t1 = run([0])
+    nh = max(1, min(w.H, int(target_s / max(t1, 1e-3))))
+    heads = list(range(nh))
+    el = run(heads)
+    value = w.T * nh / w.H / el  # tokens/s of the whole-H workload
+    return {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"fp64 token recurrence on {nh} of {w.H} heads of the full "
+                      f"{w.name} workload ({w.T} tokens), {el:.1f} s; tokens/s scaled by "
+                      f"{nh}/{w.H}"}
+
+
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if os.environ.get("GDR_BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+        dist.init_process_group(backend)
+        return dist, rank, ws
+    return None, 0, 1
+
+
+def bench_reference(args):
+    dist, rank, ws = dist_setup(args)
+    if rank != 0:
+        return 0
+    from chunked_gated_delta_gdr_gb300.inputs import make_named
+    w = make_named(args.workload)
+    # each step: the oracle on one head of the workload (a bounded sample)
+    import oracle
+    times = []
+    heads = [0]
+    for i in range(args.warmup + args.steps):
+        h = [i % w.H]
+        hk = [h[0] // (w.H // w.Hk)]
+        t0 = time.perf_counter()
+        oracle.recurrent(w.q[:, hk].contiguous(), w.k[:, hk].contiguous(),
+                         w.v[:, h].contiguous(), w.g[:, h].contiguous(),
+                         w.beta[:, h].contiguous(), w.scale,
+                         None if w.h0 is None else w.h0[:, h].contiguous(), w.cu_seqlens,
+                         want_ht=w.want_ht)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    per_step = sum(times) / len(times)
+    value = w.T / w.H / per_step
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "T": w.T, "H": w.H, "Hk": w.Hk, "d": w.dk,
+                       "n_seq": w.n_seq, "step": "one value head of the workload"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.max_threads(),
+                             "kind": "oracle",
+                             "sample": "each step runs the fp64 token recurrence on one of the "
+                                       f"{w.H} heads; tokens/s scaled by 1/{w.H}"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bench_ours(args):
+    import torch
+    dist, rank, ws = dist_setup(args)
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from chunked_gated_delta_gdr_gb300 import api
+    from chunked_gated_delta_gdr_gb300.inputs import make_named
+    w = make_named(args.workload)
+    wd = w.to(dev)
+    T, H, D, N = w.T, w.H, w.dk, w.n_seq
+    path = args.path
+    o = torch.empty(T, H, D, dtype=torch.bfloat16, device=dev)
+    ht = torch.empty(N, H, D, D, dtype=torch.float32, device=dev) if w.want_ht else None
+    wsz = api.workspace_bytes(T, N, H, D, D, path)
+    work = torch.empty(max(wsz, 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        api.chunk_fwd(wd.q, wd.k, wd.v, wd.g, wd.beta, scale=w.scale, initial_state=wd.h0,
+                      cu_seqlens=wd.cu_seqlens, output_final_state=w.want_ht, path=path,
+                      workspace=work, out=o, final_state=ht)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_wall = time.perf_counter()
+    for a, b in ev:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    per = [a.elapsed_time(b) for a, b in ev]  # ms, each step on the launching stream
+    total_ms = sum(per)
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = ws * T * args.steps / (total_ms / 1e3)
+    launches_per_step = 2 if path in ("auto", "fused") and _fused_available(api, wd, w) else 4
+    hbm, tflops, peak_kind = peaks()
+    alg_b = algorithmic_bytes(w)
+    alg_f = algorithmic_flops(w)
+    med_ms = statistics.median(per)
+    achieved_gbs = alg_b / (med_ms / 1e3) / 1e9
+    achieved_tfs = alg_f / (med_ms / 1e3) / 1e12
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if launches_per_step == 2 else "f32", "data": "synthetic",
+            "config": {"workload": w.name, "T": T, "H": H, "Hk": w.Hk, "d": D, "n_seq": N,
+                       "n_chunks": w.n_chunks(), "path": path,
+                       "l2": "inputs (2.16 GB) exceed the 129 MB L2; no flush between steps",
+                       "per_rank": "each rank runs its own copy of the workload"},
+            "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved_gbs / hbm, "peak_kind": f"{peak_kind} burst copy",
+                         "traffic": read_traffic(kernel_sha()),
+                         "algorithmic_bytes_per_launch": alg_b,
+                         "tensor": {"achieved": achieved_tfs, "peak": tflops,
+                                    "unit": "TFLOP/s", "frac": achieved_tfs / tflops,
+                                    "algorithmic_flops_per_launch": alg_f},
+                         "timed": "median CUDA-event time of the whole forward call per step "
+                                  "(chunk enumeration included)"},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+            "wall_s_timed_region": wall}
+    if not args.no_e2e:
+        line["e2e"] = bench_e2e(args, api, w, dev, path, dist)
+    if rank == 0 and not args.no_cpu_baseline and ws == 1:
+        line["cpu_baseline"] = cpu_oracle_sample(w, args.cpu_seconds)
+    if dist is not None:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def _fused_available(api, wd, w):
+    try:
+        api.chunk_fwd(wd.q[:64], wd.k[:64], wd.v[:64], wd.g[:64], wd.beta[:64],
+                      cu_seqlens=wd.cu_seqlens.new_tensor([0, 64]), path="fused")
+        return True
+    except api.nat.GdrError:
+        return False
+
+
+def bench_e2e(args, api, w, dev, path, dist):
+    """Same metric through the public API with pinned HOST inputs: every step
+    copies q, k, v, g, beta (and h0) to the device, runs, and copies o (and ht)
+    back; all inside the timed region."""
+    import torch
+    pin = lambda t: None if t is None else t.pin_memory()
+    hq, hk, hv, hg, hb, hh0 = map(pin, (w.q, w.k, w.v, w.g, w.beta, w.h0))
+    o_h = torch.empty(w.T, w.H, w.dv, dtype=torch.bfloat16).pin_memory()
+    ht_h = (torch.empty(w.n_seq, w.H, w.dk, w.dv, dtype=torch.float32).pin_memory()
+            if w.want_ht else None)
+    work = torch.empty(max(api.workspace_bytes(w.T, w.n_seq, w.H, w.dk, w.dv, path), 256),
+                       dtype=torch.uint8, device=dev)
+
+    def step():
+        api.chunk_fwd(hq, hk, hv, hg, hb, scale=w.scale, initial_state=hh0,
+                      cu_seqlens=w.cu_seqlens, output_final_state=w.want_ht, path=path,
+                      workspace=work, out=o_h, final_state=ht_h)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    steps = max(3, min(args.steps, 20))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    el = time.perf_counter() - t0
+    if dist is not None:
+        t = torch.tensor([el], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        el = float(t.item())
+    ws = dist.get_world_size() if dist is not None else 1
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg, hb, hh0, w.cu_seqlens)
+              if t is not None)
+    d2h = o_h.numel() * 2 + (ht_h.numel() * 4 if ht_h is not None else 0)
+    return {"value": ws * w.T * steps / el, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps,
+            "timed": "host wall clock around the public chunk_fwd call on pinned host tensors"}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return bench_reference(args)
+    return bench_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,237 @@
+"""Python binding of libgdr: argument marshalling only.
+
+Every step of the forward runs in libgdr's CUDA kernels; this module builds
+the C descriptors from torch tensors, allocates outputs and scratch through
+PyTorch's allocator, and passes torch's current CUDA stream.  There is no CPU
+fallback: without libgdr.so or a GB300 the calls raise.
+
+Host (CPU) tensors are accepted by ``chunk_fwd``: they are copied to the
+current CUDA device on the current stream (asynchronously when pinned), the
+forward runs there, and o / ht are copied back into host tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Tuple
+
+import torch
+
+from . import _native as nat
+
+_DT = {torch.bfloat16: nat.GDR_BF16, torch.float32: nat.GDR_F32, torch.int32: nat.GDR_I32}
+
+
+class _Desc:
+    """A gdr_tensor_t for a torch tensor (keeps the strides array alive)."""
+
+    def __init__(self, t: torch.Tensor):
+        if t.dtype not in _DT:
+            raise TypeError(f"unsupported dtype {t.dtype}")
+        if t.dim() < 1 or t.dim() > 4:
+            raise ValueError("tensors must have 1..4 dims")
+        self.strides = (ctypes.c_int64 * t.dim())(*t.stride())
+        shape = (ctypes.c_int64 * 4)(*(list(t.shape) + [0] * (4 - t.dim())))
+        self.c = nat.GdrTensor(ctypes.c_void_p(t.data_ptr() if t.numel() else 0), _DT[t.dtype],
+                               t.dim(), shape,
+                               ctypes.cast(self.strides, ctypes.POINTER(ctypes.c_int64)))
+
+    @property
+    def ref(self):
+        return ctypes.byref(self.c)
+
+
+def _d(t: Optional[torch.Tensor]):
+    return None if t is None else _Desc(t)
+
+
+def _ref(d):
+    return None if d is None else d.ref
+
+
+def _stream(stream=None) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None or t.numel() == 0 else ctypes.c_void_p(t.data_ptr())
+
+
+def chunk_count_bound(T: int, n_seq: int) -> int:
+    return int(nat.lib().gdr_chunk_count_bound(T, n_seq))
+
+
+def workspace_bytes(T: int, n_seq: int, H: int, dk: int, dv: int, path: str = "auto") -> int:
+    return int(nat.lib().gdr_chunk_fwd_workspace_bytes(T, n_seq, H, dk, dv, nat.PATHS[path]))
+
+
+def stage_workspace_bytes(T: int, n_seq: int) -> int:
+    return int(nat.lib().gdr_stage_workspace_bytes(T, n_seq))
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+              beta: torch.Tensor, scale: Optional[float] = None,
+              initial_state: Optional[torch.Tensor] = None,
+              cu_seqlens: Optional[torch.Tensor] = None, output_final_state: bool = False,
+              path: str = "auto", workspace: Optional[torch.Tensor] = None,
+              out: Optional[torch.Tensor] = None, final_state: Optional[torch.Tensor] = None,
+              stream: Optional[torch.cuda.Stream] = None
+              ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Chunked gated delta rule forward (libgdr ``gdr_chunk_fwd_ws``).
+
+    q, k [T, Hk, dk] bf16; v [T, H, dv] bf16; g [T, H] f32; beta [T, H] bf16;
+    initial_state [N, H, dk, dv] f32 or None; cu_seqlens [N + 1] int32 (None:
+    one segment of T tokens).  Returns (o [T, H, dv] bf16, ht or None).
+    """
+    host = q.device.type == "cpu"
+    if host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        mv = lambda t: None if t is None else t.to(dev, non_blocking=True)
+        q, k, v, g, beta, initial_state = map(mv, (q, k, v, g, beta, initial_state))
+        cu_seqlens = mv(cu_seqlens)
+    dev = q.device
+    T, H, dv = q.shape[0], v.shape[1], v.shape[2]
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    n_seq = cu_seqlens.numel() - 1
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    o = torch.empty(T, H, dv, dtype=torch.bfloat16, device=dev) if (out is None or host) else out
+    ht = None
+    if output_final_state:
+        ht = (torch.empty(n_seq, H, q.shape[-1], dv, dtype=torch.float32, device=dev)
+              if (final_state is None or host) else final_state)
+    if workspace is None:
+        workspace = _workspace(workspace_bytes(T, n_seq, H, q.shape[-1], dv, path), dev)
+    ds = [_Desc(t) for t in (q, k, v, g, beta)]
+    dh0, do, dht = _d(initial_state), _Desc(o), _d(ht)
+    rc = nat.lib().gdr_chunk_fwd_ws(
+        ds[0].ref, ds[1].ref, ds[2].ref, ds[3].ref, ds[4].ref, ctypes.c_float(scale),
+        _ref(dh0), _ptr(cu_seqlens), n_seq, do.ref, _ref(dht), nat.PATHS[path],
+        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream(stream))
+    nat.check(rc, "gdr_chunk_fwd_ws")
+    if host:
+        o_h = out if out is not None else torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        o_h.copy_(o, non_blocking=True)
+        ht_h = None
+        if ht is not None:
+            ht_h = final_state if final_state is not None else torch.empty(
+                ht.shape, dtype=ht.dtype, pin_memory=True)
+            ht_h.copy_(ht, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return o_h, ht_h
+    return o, ht
+
+
+def chunk_fwd_alloc(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
+                    output_final_state=False, stream=None):
+    """Same as ``chunk_fwd`` on device tensors, but through ``gdr_chunk_fwd``,
+    which takes its scratch with cudaMallocAsync on the stream."""
+    dev = q.device
+    T, H, dv = q.shape[0], v.shape[1], v.shape[2]
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    n_seq = cu_seqlens.numel() - 1
+    scale = q.shape[-1] ** -0.5 if scale is None else scale
+    o = torch.empty(T, H, dv, dtype=torch.bfloat16, device=dev)
+    ht = (torch.empty(n_seq, H, q.shape[-1], dv, dtype=torch.float32, device=dev)
+          if output_final_state else None)
+    ds = [_Desc(t) for t in (q, k, v, g, beta)]
+    dh0, do, dht = _d(initial_state), _Desc(o), _d(ht)
+    rc = nat.lib().gdr_chunk_fwd(ds[0].ref, ds[1].ref, ds[2].ref, ds[3].ref, ds[4].ref,
+                                 ctypes.c_float(scale), _ref(dh0), _ptr(cu_seqlens), n_seq,
+                                 do.ref, _ref(dht), _stream(stream))
+    nat.check(rc, "gdr_chunk_fwd")
+    return o, ht
+
+
+# ---------------------------------------------------------------- stages
+
+def chunk_index(cu_seqlens: torch.Tensor, T: int, stream=None):
+    """Device chunk enumeration: (seg_table [N, 4], chunk_table [bound, 4], n_chunks [1])."""
+    dev = cu_seqlens.device
+    n_seq = cu_seqlens.numel() - 1
+    seg = torch.empty(max(n_seq, 1), 4, dtype=torch.int32, device=dev)
+    chunks = torch.empty(max(chunk_count_bound(T, n_seq), 1), 4, dtype=torch.int32, device=dev)
+    n = torch.empty(1, dtype=torch.int32, device=dev)
+    rc = nat.lib().gdr_chunk_index(_ptr(cu_seqlens), n_seq, T, _ptr(seg), _ptr(chunks),
+                                   _ptr(n), _stream(stream))
+    nat.check(rc, "gdr_chunk_index")
+    return seg[:n_seq], chunks[:chunk_count_bound(T, n_seq)], n
+
+
+def chunk_prep(k, v, g, beta, cu_seqlens, stream=None):
+    """Stage 1: returns (w [T, H, dk] bf16, u [T, H, dv] bf16, gcum [T, H] f32)."""
+    dev = k.device
+    T, H, dk, dv = k.shape[0], v.shape[1], k.shape[2], v.shape[2]
+    n_seq = cu_seqlens.numel() - 1
+    w = torch.zeros(T, H, dk, dtype=torch.bfloat16, device=dev)
+    u = torch.zeros(T, H, dv, dtype=torch.bfloat16, device=dev)
+    gc = torch.zeros(T, H, dtype=torch.float32, device=dev)
+    ws = _workspace(stage_workspace_bytes(T, n_seq), dev)
+    d = [_Desc(t) for t in (k, v, g, beta, w, u, gc)]
+    rc = nat.lib().gdr_chunk_prep(d[0].ref, d[1].ref, d[2].ref, d[3].ref, _ptr(cu_seqlens),
+                                  n_seq, d[4].ref, d[5].ref, d[6].ref,
+                                  ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(stream))
+    nat.check(rc, "gdr_chunk_prep")
+    return w, u, gc
+
+
+def state_scan(k, w, u, gcum, initial_state, cu_seqlens, output_final_state=True, stream=None):
+    """Stage 2: returns (h [bound, H, dk, dv] bf16, v_new [T, H, dv] bf16, ht or None)."""
+    dev = k.device
+    T, H, dk, dv = k.shape[0], w.shape[1], k.shape[2], u.shape[2]
+    n_seq = cu_seqlens.numel() - 1
+    h = torch.zeros(max(chunk_count_bound(T, n_seq), 0), H, dk, dv, dtype=torch.bfloat16,
+                    device=dev)
+    vn = torch.zeros(T, H, dv, dtype=torch.bfloat16, device=dev)
+    ht = (torch.zeros(n_seq, H, dk, dv, dtype=torch.float32, device=dev)
+          if output_final_state else None)
+    ws = _workspace(stage_workspace_bytes(T, n_seq), dev)
+    d = [_Desc(t) for t in (k, w, u, gcum, h, vn)]
+    dh0, dht = _d(initial_state), _d(ht)
+    rc = nat.lib().gdr_state_scan(d[0].ref, d[1].ref, d[2].ref, d[3].ref, _ref(dh0),
+                                  _ptr(cu_seqlens), n_seq, d[4].ref, d[5].ref, _ref(dht),
+                                  ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(stream))
+    nat.check(rc, "gdr_state_scan")
+    return h, vn, ht
+
+
+def chunk_out(q, k, v_new, h, gcum, scale, cu_seqlens, stream=None):
+    """Stage 3: returns o [T, H, dv] bf16 (uncovered tokens zero)."""
+    dev = q.device
+    T, H, dv = q.shape[0], v_new.shape[1], v_new.shape[2]
+    n_seq = cu_seqlens.numel() - 1
+    o = torch.zeros(T, H, dv, dtype=torch.bfloat16, device=dev)
+    ws = _workspace(stage_workspace_bytes(T, n_seq), dev)
+    d = [_Desc(t) for t in (q, k, v_new, h, gcum, o)]
+    rc = nat.lib().gdr_chunk_out(d[0].ref, d[1].ref, d[2].ref, d[3].ref, d[4].ref,
+                                 ctypes.c_float(scale), _ptr(cu_seqlens), n_seq, d[5].ref,
+                                 ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(stream))
+    nat.check(rc, "gdr_chunk_out")
+    return o
+
+
+def check_cu_seqlens(cu_seqlens: torch.Tensor, T: int, stream=None) -> Tuple[int, int]:
+    """(number of malformed offsets, index of the first one or -1); synchronises."""
+    n_bad = ctypes.c_int32(0)
+    first = ctypes.c_int32(0)
+    rc = nat.lib().gdr_debug_check_cu_seqlens(_ptr(cu_seqlens), cu_seqlens.numel() - 1, T,
+                                              ctypes.byref(n_bad), ctypes.byref(first),
+                                              _stream(stream))
+    nat.check(rc, "gdr_debug_check_cu_seqlens")
+    return n_bad.value, first.value
+
+
+def device_status() -> int:
+    s = ctypes.c_int32(0)
+    nat.check(nat.lib().gdr_device_status(ctypes.byref(s)), "gdr_device_status")
+    return s.value
+
+
+def clear_device_status() -> None:
+    nat.check(nat.lib().gdr_clear_device_status(), "gdr_clear_device_status")

@@ -1,0 +1,103 @@
+// gdr_internal.cuh -- shared definitions of the libgdr CUDA sources (not installed).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdr.h"
+
+namespace gdr {
+
+constexpr int kChunk = 64;  // tokens per chunk
+
+// Per-segment entry of the chunk enumeration: sanitised bounds [start, end),
+// id of the segment's first chunk, number of chunks.
+struct SegInfo {
+  int32_t start, end, chunk_off, n_chunks;
+};
+
+// Per-chunk entry: owning segment, first token, token count (1..64).
+struct ChunkInfo {
+  int32_t seq, start, len, pad;
+};
+
+// A [rows, heads, dim] tensor with a contiguous innermost dim, or a [rows, heads]
+// tensor (dim stride unused).  Strides are in elements.
+struct View {
+  void *p;
+  int64_t st;  // token (row) stride
+  int64_t sh;  // head stride
+};
+
+__host__ __device__ inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+inline int64_t chunk_bound(int64_t T, int32_t n_seq) { return ceil_div64(T, kChunk) + n_seq; }
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+__device__ __forceinline__ float ldbf(const void *p, int64_t i) {
+  return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[i]);
+}
+
+__device__ __forceinline__ void stbf(void *p, int64_t i, float x) {
+  reinterpret_cast<__nv_bfloat16 *>(p)[i] = __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float ldf(const void *p, int64_t i) {
+  return reinterpret_cast<const float *>(p)[i];
+}
+
+// ---- host-side launchers implemented in the .cu files ----
+
+// Chunk enumeration (gdr_index.cu).
+cudaError_t launch_chunk_index(const int32_t *cu, int32_t n_seq, int64_t T, SegInfo *seg,
+                               ChunkInfo *chunks, int64_t chunk_cap, int32_t *n_chunks,
+                               cudaStream_t stream);
+cudaError_t launch_check_cu(const int32_t *cu, int32_t n_seq, int64_t T, int32_t *out2,
+                            cudaStream_t stream);
+
+// Stage kernels (gdr_staged.cu).  All views are validated by the caller.
+struct StageShapes {
+  int64_t T;
+  int32_t n_seq, Hk, H, D;
+  int64_t chunk_cap;
+};
+
+cudaError_t launch_prep(const StageShapes &s, View k, View v, View g, View beta, View w,
+                        View u, View gcum, const SegInfo *seg, const ChunkInfo *chunks,
+                        const int32_t *n_chunks, cudaStream_t stream);
+cudaError_t launch_scan(const StageShapes &s, View k, View w, View u, View gcum,
+                        const float *h0, void *h, View v_new, float *ht, const SegInfo *seg,
+                        cudaStream_t stream);
+cudaError_t launch_out(const StageShapes &s, View q, View k, View v_new, const void *h,
+                       View gcum, float scale, View o, const SegInfo *seg,
+                       const ChunkInfo *chunks, const int32_t *n_chunks, cudaStream_t stream);
+
+// Fused persistent kernel (gdr_fused.cu).
+struct FusedArgs {
+  int64_t T;
+  int32_t n_seq, Hk, H, D;
+  const void *q, *k, *v;
+  int64_t q_st, q_sh, k_st, k_sh, v_st, v_sh;
+  const float *g;
+  int64_t g_st, g_sh;
+  const void *beta;
+  int64_t b_st, b_sh;
+  float scale;
+  const float *h0;
+  void *o;
+  int64_t o_st, o_sh;
+  float *ht;
+  const SegInfo *seg;
+  void *workspace;  // fused-path scratch (work list etc.)
+};
+bool fused_supported(const FusedArgs &a);
+size_t fused_workspace_bytes(int64_t T, int32_t n_seq, int32_t H);
+cudaError_t launch_fused(const FusedArgs &a, cudaStream_t stream);
+
+// Device status word (gdr_fused.cu).
+cudaError_t read_device_status(int32_t *out);
+cudaError_t clear_device_status();
+
+}  // namespace gdr

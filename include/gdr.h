@@ -1,0 +1,208 @@
+/*
+ * gdr.h -- C ABI of libgdr: the chunked gated delta rule forward on GB300 (sm_103a).
+ *
+ * The operation (per packed segment n and value head h, state S of dk x dv):
+ *
+ *     S_t = exp(g_t) (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T,   S_{start-1} = h0[n,h] or 0
+ *     o_t = scale * S_t^T q_t,                                          ht[n,h] = S_last
+ *
+ * evaluated chunkwise with chunks of 64 tokens, the chunk size of FlashQLA's
+ * chunk_gated_delta_rule varlen path ("Findings from integrating FlashQLA's
+ * Blackwell GDN kernels into a JAX trainer", section 1: prepare_chunk_indices(cu, 64);
+ * "FlashQLA GDN backend produces different tokens from FLA Triton on
+ * correctness-test prompts", Setup: chunk_size=64, varlen API).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every data pointer is a DEVICE pointer on the current CUDA device, except
+ *   the gdr_tensor_t structs themselves and their `strides` arrays, which live
+ *   in host memory and are only read during the call.  The caller owns every
+ *   buffer; the library keeps no pointer after a call returns and has no
+ *   cache keyed on addresses (the stale-cache failure in "Findings ...",
+ *   section 1, cannot occur).
+ * - Layouts (row-major by default):
+ *       q, k   [T, Hk, dk]  bf16          v, o   [T, H, dv]  bf16
+ *       g      [T, H]       f32 (natural-log decay, exp(g) multiplies the state)
+ *       beta   [T, H]       bf16          h0, ht [N, H, dk, dv] f32 (row = key dim)
+ *   H % Hk == 0 and value head h reads query/key head h / (H / Hk).
+ *   dk == dv, with dk in {64, 128}.
+ * - `strides == NULL` means compact row-major, as DLPack defines it ("Findings
+ *   ...", section 3: stubs that rejected NULL strides).  Explicit strides are
+ *   in elements; the innermost stride must be 1.  h0/ht must be compact.
+ * - cu_seqlens: DEVICE int32 array of n_seq + 1 offsets into the token axis.
+ *   It is never read on the host.  Offsets are clamped to [0, T] and made
+ *   non-decreasing by a running maximum, so a malformed array cannot cause an
+ *   out-of-bounds access.  Repeated offsets are length-0 ("ghost") segments
+ *   ("Findings ...", section 2): they write no o and, when ht is requested,
+ *   ht[n] = h0[n] (or zeros).  Tokens outside every segment are not written.
+ * - Return value: GDR_OK (0) or a negative gdr_status code.  Nothing is
+ *   thrown across the ABI.  Kernels are enqueued on `stream` and the call does
+ *   not synchronise; asynchronous device errors surface on the stream.
+ */
+#ifndef GDR_H_
+#define GDR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types of gdr_tensor_t::dtype. */
+enum gdr_dtype { GDR_BF16 = 1, GDR_F32 = 2, GDR_I32 = 3 };
+
+/* Status codes. */
+enum gdr_status {
+  GDR_OK = 0,
+  GDR_ERR_NULL = -1,      /* a required pointer or descriptor is NULL          */
+  GDR_ERR_DTYPE = -2,     /* wrong element type                                 */
+  GDR_ERR_SHAPE = -3,     /* wrong rank or inconsistent extents                 */
+  GDR_ERR_STRIDE = -4,    /* innermost stride != 1, negative stride, non-compact state */
+  GDR_ERR_DIM = -5,       /* head dimension not supported (dk == dv in {64,128}) */
+  GDR_ERR_HEADS = -6,     /* H % Hk != 0                                        */
+  GDR_ERR_NSEQ = -7,      /* n_seq < 0 or n_seq inconsistent with h0/ht         */
+  GDR_ERR_WORKSPACE = -8, /* workspace NULL, too small or not 256-byte aligned   */
+  GDR_ERR_PATH = -9,      /* unknown path, or FUSED requested but unsupported    */
+  GDR_ERR_CUDA = -10,     /* a CUDA runtime call or kernel launch failed         */
+  GDR_ERR_ALIGN = -11,    /* a base pointer or row stride is not 16-byte aligned */
+  GDR_ERR_DEVICE = -12    /* the current device is not sm_103 (GB300)            */
+};
+
+/* Execution paths of the forward. */
+enum gdr_path {
+  GDR_PATH_AUTO = 0,   /* fused when its alignment preconditions hold, else staged */
+  GDR_PATH_FUSED = 1,  /* one persistent kernel per call; intermediates stay on chip */
+  GDR_PATH_STAGED = 2  /* the three stages as separate kernels with HBM intermediates */
+};
+
+typedef struct gdr_tensor {
+  void *data;             /* device pointer to element [0,...,0]           */
+  int32_t dtype;          /* enum gdr_dtype                                  */
+  int32_t ndim;           /* 1..4                                            */
+  int64_t shape[4];       /* extents, outermost first                        */
+  const int64_t *strides; /* host array of ndim strides in elements, or NULL */
+} gdr_tensor_t;
+
+/*
+ * gdr_chunk_fwd -- the whole forward: q, k, v, g, beta (+ optional h0) -> o (+ optional ht).
+ *
+ *   q, k    [T, Hk, dk] bf16; v [T, H, dv] bf16; g [T, H] f32; beta [T, H] bf16
+ *   scale   multiplies the output (o = scale * S^T q)
+ *   h0      [n_seq, H, dk, dv] f32 initial states, or NULL for zero states
+ *   cu_seqlens, n_seq   see the conventions above
+ *   o       [T, H, dv] bf16 output (round-to-nearest-even); covered tokens only
+ *   ht      [n_seq, H, dk, dv] f32 final states, or NULL to skip them
+ *           (FlashQLA drops dead h0/ht parameters in this case: "Findings ...", section 4)
+ *
+ * Runs GDR_PATH_AUTO.  Scratch memory is taken with cudaMallocAsync on `stream`
+ * and released with cudaFreeAsync on the same stream.  Errors: any gdr_status.
+ */
+int gdr_chunk_fwd(const gdr_tensor_t *q, const gdr_tensor_t *k, const gdr_tensor_t *v,
+                  const gdr_tensor_t *g, const gdr_tensor_t *beta, float scale,
+                  const gdr_tensor_t *h0, const int32_t *cu_seqlens, int32_t n_seq,
+                  gdr_tensor_t *o, gdr_tensor_t *ht, cudaStream_t stream);
+
+/* Bytes of device scratch gdr_chunk_fwd_ws needs for these extents and path
+ * (GDR_PATH_AUTO sizes for the larger of the two).  Never fails; returns 0 for
+ * negative arguments. */
+size_t gdr_chunk_fwd_workspace_bytes(int64_t T, int32_t n_seq, int32_t H, int32_t dk,
+                                     int32_t dv, int32_t path);
+
+/*
+ * gdr_chunk_fwd_ws -- gdr_chunk_fwd with a caller-owned workspace and an explicit path.
+ *   workspace   device pointer, 256-byte aligned, at least
+ *               gdr_chunk_fwd_workspace_bytes(T, n_seq, H, dk, dv, path) bytes.
+ *               Stream-ordered: it may be reused once the call's work on `stream` is done.
+ * Errors: as gdr_chunk_fwd, plus GDR_ERR_WORKSPACE and GDR_ERR_PATH.
+ */
+int gdr_chunk_fwd_ws(const gdr_tensor_t *q, const gdr_tensor_t *k, const gdr_tensor_t *v,
+                     const gdr_tensor_t *g, const gdr_tensor_t *beta, float scale,
+                     const gdr_tensor_t *h0, const int32_t *cu_seqlens, int32_t n_seq,
+                     gdr_tensor_t *o, gdr_tensor_t *ht, int32_t path, void *workspace,
+                     size_t workspace_bytes, cudaStream_t stream);
+
+/* Upper bound on the number of 64-token chunks: ceil(T / 64) + n_seq. */
+int64_t gdr_chunk_count_bound(int64_t T, int32_t n_seq);
+
+/* Bytes of device scratch each stage entry point below needs (chunk tables). */
+size_t gdr_stage_workspace_bytes(int64_t T, int32_t n_seq);
+
+/*
+ * Chunk enumeration from cu_seqlens, on the device.
+ *   seg_table   [n_seq, 4] int32 out: (start, end, first chunk id, chunk count) per segment
+ *   chunk_table [gdr_chunk_count_bound(T, n_seq), 4] int32 out: (segment, first token,
+ *               length 1..64, 0) per chunk id; ids are assigned segment by segment.
+ *   n_chunks    device int32 out: the number of chunks.
+ * Errors: GDR_ERR_NULL, GDR_ERR_NSEQ, GDR_ERR_SHAPE (T < 0), GDR_ERR_CUDA.
+ */
+int gdr_chunk_index(const int32_t *cu_seqlens, int32_t n_seq, int64_t T, int32_t *seg_table,
+                    int32_t *chunk_table, int32_t *n_chunks, cudaStream_t stream);
+
+/*
+ * Stage 1, gdr_chunk_prep: per (chunk, value head) with chunk-local index i, j:
+ *   G_i  = sum_{t<=i} g_t (chunk-local inclusive cumsum)
+ *   A_ij = beta_i exp(G_i - G_j) k_i.k_j (j < i), Tm = (I + A)^-1
+ *   W = Tm diag(beta exp(G)) K,  U = Tm diag(beta) V
+ * Outputs (compact, covered tokens only): w [T, H, dk] bf16, u [T, H, dv] bf16,
+ * gcum [T, H] f32.  workspace: gdr_stage_workspace_bytes(T, n_seq) bytes.
+ */
+int gdr_chunk_prep(const gdr_tensor_t *k, const gdr_tensor_t *v, const gdr_tensor_t *g,
+                   const gdr_tensor_t *beta, const int32_t *cu_seqlens, int32_t n_seq,
+                   gdr_tensor_t *w, gdr_tensor_t *u, gdr_tensor_t *gcum, void *workspace,
+                   size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Stage 2, gdr_state_scan: per (segment, value head), sequential over chunks, fp32 state:
+ *   h[c] = S (bf16);  V' = U - W S;  S <- exp(G_last) S + (diag(exp(G_last - G)) K)^T V'
+ * Inputs: k [T, Hk, dk] bf16, w/u/gcum from stage 1, h0 (or NULL).
+ * Outputs: h [gdr_chunk_count_bound, H, dk, dv] bf16 indexed by chunk id,
+ * v_new [T, H, dv] bf16 (V'), ht (or NULL).  workspace as for stage 1.
+ */
+int gdr_state_scan(const gdr_tensor_t *k, const gdr_tensor_t *w, const gdr_tensor_t *u,
+                   const gdr_tensor_t *gcum, const gdr_tensor_t *h0,
+                   const int32_t *cu_seqlens, int32_t n_seq, gdr_tensor_t *h,
+                   gdr_tensor_t *v_new, gdr_tensor_t *ht, void *workspace,
+                   size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Stage 3, gdr_chunk_out: per (chunk, value head):
+ *   O = scale [ diag(exp(G)) Q h[c] + (M o Q K^T) V' ],  M_ij = exp(G_i - G_j) for j <= i, else 0
+ * Inputs: q, k [T, Hk, dk] bf16, v_new [T, H, dv] bf16, h and gcum as above.
+ * Output: o [T, H, dv] bf16, covered tokens only.  workspace as for stage 1.
+ */
+int gdr_chunk_out(const gdr_tensor_t *q, const gdr_tensor_t *k, const gdr_tensor_t *v_new,
+                  const gdr_tensor_t *h, const gdr_tensor_t *gcum, float scale,
+                  const int32_t *cu_seqlens, int32_t n_seq, gdr_tensor_t *o, void *workspace,
+                  size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Debug check of cu_seqlens (synchronises `stream`): *n_bad receives the number of
+ * offsets that are negative, above T, or below their predecessor, and *first_bad the
+ * index of the first such offset (-1 if none).  Errors: GDR_ERR_NULL, GDR_ERR_NSEQ, GDR_ERR_CUDA.
+ */
+int gdr_debug_check_cu_seqlens(const int32_t *cu_seqlens, int32_t n_seq, int64_t T,
+                               int32_t *n_bad, int32_t *first_bad, cudaStream_t stream);
+
+/*
+ * Device status word of the fused kernel.  Every bounded wait inside the fused
+ * kernel that runs out sets a nonzero code here (it then releases what it holds and
+ * returns instead of hanging).  gdr_device_status synchronises the current device and
+ * reads the word; gdr_clear_device_status resets it.  0 means no wait ran out.
+ */
+int gdr_device_status(int32_t *status_out);
+int gdr_clear_device_status(void);
+
+/* Human-readable text for a gdr_status code (static storage). */
+const char *gdr_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int gdr_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDR_H_ */
