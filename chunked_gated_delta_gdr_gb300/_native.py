@@ -15,7 +15,7 @@ STATUS = {
     0: "GDR_OK", -1: "GDR_ERR_NULL", -2: "GDR_ERR_DTYPE", -3: "GDR_ERR_SHAPE",
     -4: "GDR_ERR_STRIDE", -5: "GDR_ERR_DIM", -6: "GDR_ERR_HEADS", -7: "GDR_ERR_NSEQ",
     -8: "GDR_ERR_WORKSPACE", -9: "GDR_ERR_PATH", -10: "GDR_ERR_CUDA", -11: "GDR_ERR_ALIGN",
-    -12: "GDR_ERR_DEVICE",
+    -12: "GDR_ERR_DEVICE", -13: "GDR_ERR_SCRATCH_LIMIT",
 }
 
 # Every function the header declares, with its ctypes signature.
@@ -41,6 +41,7 @@ SIGNATURES = {
     "gdr_chunk_prep": (ctypes.c_int, [_T, _T, _T, _T, _vp, _i32, _T, _T, _T, _vp, _sz, _vp]),
     "gdr_state_scan": (ctypes.c_int, [_T, _T, _T, _T, _T, _vp, _i32, _T, _T, _T, _vp, _sz, _vp]),
     "gdr_chunk_out": (ctypes.c_int, [_T, _T, _T, _T, _T, _f32, _vp, _i32, _T, _vp, _sz, _vp]),
+    "gdr_chunk_out_noalloc": (ctypes.c_int, [_T, _T, _T, _T, _T, _f32, _vp, _i32, _T, _vp]),
     "gdr_debug_check_cu_seqlens": (ctypes.c_int, [_vp, _i32, _i64, _vp, _vp, _vp]),
     "gdr_device_status": (ctypes.c_int, [_vp]),
     "gdr_clear_device_status": (ctypes.c_int, []),

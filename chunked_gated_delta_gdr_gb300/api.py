@@ -216,6 +216,22 @@ def chunk_out(q, k, v_new, h, gcum, scale, cu_seqlens, stream=None):
     return o
 
 
+def chunk_out_noalloc(q, k, v_new, h, gcum, scale, cu_seqlens, out=None, stream=None):
+    """Stage 3 through ``gdr_chunk_out_noalloc``: no device allocation inside the
+    library (its chunk tables live in a static 4 MiB device array).  ``out`` may be
+    a preallocated o [T, H, dv] bf16; otherwise one is allocated here by torch."""
+    dev = q.device
+    T, H, dv = q.shape[0], v_new.shape[1], v_new.shape[2]
+    n_seq = cu_seqlens.numel() - 1
+    o = torch.zeros(T, H, dv, dtype=torch.bfloat16, device=dev) if out is None else out
+    d = [_Desc(t) for t in (q, k, v_new, h, gcum, o)]
+    rc = nat.lib().gdr_chunk_out_noalloc(d[0].ref, d[1].ref, d[2].ref, d[3].ref, d[4].ref,
+                                         ctypes.c_float(scale), _ptr(cu_seqlens), n_seq,
+                                         d[5].ref, _stream(stream))
+    nat.check(rc, "gdr_chunk_out_noalloc")
+    return o
+
+
 def check_cu_seqlens(cu_seqlens: torch.Tensor, T: int, stream=None) -> Tuple[int, int]:
     """(number of malformed offsets, index of the first one or -1); synchronises."""
     n_bad = ctypes.c_int32(0)

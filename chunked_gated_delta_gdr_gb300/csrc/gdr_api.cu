@@ -1,6 +1,7 @@
 // gdr_api.cu -- the extern "C" boundary of libgdr: descriptor validation,
 // workspace carving and stream-ordered launches.  No host synchronisation
 // except in gdr_debug_check_cu_seqlens and gdr_device_status.
+#include <mutex>
 #include <string.h>
 
 #include "gdr_internal.cuh"
@@ -262,6 +263,8 @@ const char *gdr_status_string(int status) {
     case GDR_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
     case GDR_ERR_ALIGN: return "a base pointer or row stride is not 16-byte aligned";
     case GDR_ERR_DEVICE: return "the current device is not sm_103 (GB300)";
+    case GDR_ERR_SCRATCH_LIMIT:
+      return "problem too large for the 4 MiB static scratch of gdr_chunk_out_noalloc";
     default: return "unknown status";
   }
 }
@@ -506,3 +509,76 @@ int gdr_clear_device_status(void) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// gdr_chunk_out_noalloc: stage 3 with its chunk tables in a static device array,
+// for callers that cannot allocate device memory.  Host code may not pass the
+// array's name to a kernel (in host code it names a host-side shadow); the
+// device address is looked up once per device with cudaGetSymbolAddress.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = GDR_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device (looked up on first use).
+int noalloc_scratch(void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDR_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return GDR_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return GDR_OK;
+}
+
+}  // namespace
+
+extern "C" int gdr_chunk_out_noalloc(const gdr_tensor_t *q, const gdr_tensor_t *k,
+                                     const gdr_tensor_t *v_new, const gdr_tensor_t *h,
+                                     const gdr_tensor_t *gcum, float scale,
+                                     const int32_t *cu_seqlens, int32_t n_seq, gdr_tensor_t *o,
+                                     cudaStream_t stream) {
+  Desc Q, K, Vn, Hd, Gc, O;
+  int r;
+  if ((r = read_desc(q, GDR_BF16, 3, &Q)) || (r = read_desc(k, GDR_BF16, 3, &K)) ||
+      (r = read_desc(v_new, GDR_BF16, 3, &Vn)) || (r = read_desc(h, GDR_BF16, 4, &Hd)) ||
+      (r = read_desc(gcum, GDR_F32, 2, &Gc)) || (r = read_desc(o, GDR_BF16, 3, &O)))
+    return r;
+  const int64_t T = Q.shape[0], Hk = Q.shape[1], D = Q.shape[2], H = Vn.shape[1];
+  for (int i = 0; i < 3; ++i)
+    if (K.shape[i] != Q.shape[i]) return GDR_ERR_SHAPE;
+  if (Vn.shape[0] != T || Gc.shape[0] != T || O.shape[0] != T) return GDR_ERR_SHAPE;
+  if (Gc.shape[1] != H || O.shape[1] != H || Vn.shape[2] != D || O.shape[2] != D)
+    return GDR_ERR_SHAPE;
+  if (D != 64 && D != 128) return GDR_ERR_DIM;
+  if (Hk <= 0 || H <= 0) return GDR_ERR_SHAPE;
+  if (H % Hk) return GDR_ERR_HEADS;
+  if (T > 0x7fffffffLL) return GDR_ERR_SHAPE;
+  if (n_seq < 0) return GDR_ERR_NSEQ;
+  if (n_seq > 0 && !cu_seqlens) return GDR_ERR_NULL;
+  const int64_t cap = chunk_bound(T, n_seq);
+  if (Hd.shape[0] < cap || Hd.shape[1] != H || Hd.shape[2] != D || Hd.shape[3] != D)
+    return GDR_ERR_SHAPE;
+  if (!compact(Hd)) return GDR_ERR_STRIDE;
+  if ((r = device_ok())) return r;
+  if (n_seq == 0) return GDR_OK;
+  if (carve_index(nullptr, T, n_seq).bytes > kNoAllocScratchBytes) return GDR_ERR_SCRATCH_LIMIT;
+  void *scratch = nullptr;
+  if ((r = noalloc_scratch(&scratch))) return r;
+  const IndexWs ix = carve_index(scratch, T, n_seq);
+  const StageShapes s{T, n_seq, (int32_t)Hk, (int32_t)H, (int32_t)D, cap};
+  cudaError_t e = launch_chunk_index(cu_seqlens, n_seq, T, ix.seg, ix.chunks, cap,
+                                     ix.n_chunks, stream);
+  if (e == cudaSuccess)
+    e = launch_out(s, view_of(Q), view_of(K), view_of(Vn), Hd.p, view_of(Gc), scale,
+                   view_of(O), ix.seg, ix.chunks, ix.n_chunks, stream);
+  return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}

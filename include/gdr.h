@@ -68,7 +68,8 @@ enum gdr_status {
   GDR_ERR_PATH = -9,      /* unknown path, or FUSED requested but unsupported    */
   GDR_ERR_CUDA = -10,     /* a CUDA runtime call or kernel launch failed         */
   GDR_ERR_ALIGN = -11,    /* a base pointer or row stride is not 16-byte aligned */
-  GDR_ERR_DEVICE = -12    /* the current device is not sm_103 (GB300)            */
+  GDR_ERR_DEVICE = -12,   /* the current device is not sm_103 (GB300)            */
+  GDR_ERR_SCRATCH_LIMIT = -13 /* problem too large for gdr_chunk_out_noalloc's static scratch */
 };
 
 /* Execution paths of the forward. */
@@ -194,6 +195,39 @@ int gdr_debug_check_cu_seqlens(const int32_t *cu_seqlens, int32_t n_seq, int64_t
  */
 int gdr_device_status(int32_t *status_out);
 int gdr_clear_device_status(void);
+
+/*
+ * gdr_chunk_out_noalloc -- gdr_chunk_out for callers that cannot allocate device memory.
+ *
+ * The papers behind this library have no counterpart of this entry point; it exists for
+ * embedders that may not call cudaMalloc or hand out a workspace: engines with a fixed,
+ * pre-planned memory budget, custom-call hosts that own every buffer, or code that must
+ * not touch the allocator while it runs.  It computes exactly what gdr_chunk_out computes,
+ * with the same arguments minus the workspace, and calls no cudaMalloc, cudaFree or
+ * allocating library routine.
+ *
+ * Scratch: the chunk tables (segment table, chunk table, chunk count) live in one static
+ * device array of GDR_NOALLOC_SCRATCH_BYTES (4 MiB) inside libgdr; every GPU that loads
+ * the library holds that array until the process exits.  A problem needs
+ * 256 + 16 * max(n_seq, 1) + 16 * gdr_chunk_count_bound(T, n_seq) bytes, each term rounded
+ * up to 256; larger problems return GDR_ERR_SCRATCH_LIMIT (roughly 260k chunks).
+ * The tables are rewritten completely by every call, so nothing needs clearing between
+ * calls.  Every call on a device shares the same array: calls whose work overlaps on the
+ * GPU (different streams without ordering between them) race and may produce wrong
+ * output; order them on one stream or with events.
+ *
+ * Set-up: the first call on each device (with that device current) looks up the array's
+ * device address with cudaGetSymbolAddress and caches it; make that first call before
+ * any stream capture on that device.
+ *
+ * Errors: as gdr_chunk_out (without GDR_ERR_WORKSPACE), plus GDR_ERR_SCRATCH_LIMIT, and
+ * GDR_ERR_CUDA if the address lookup fails.
+ */
+#define GDR_NOALLOC_SCRATCH_BYTES (4u << 20)
+int gdr_chunk_out_noalloc(const gdr_tensor_t *q, const gdr_tensor_t *k,
+                          const gdr_tensor_t *v_new, const gdr_tensor_t *h,
+                          const gdr_tensor_t *gcum, float scale, const int32_t *cu_seqlens,
+                          int32_t n_seq, gdr_tensor_t *o, cudaStream_t stream);
 
 /* Human-readable text for a gdr_status code (static storage). */
 const char *gdr_status_string(int status);
