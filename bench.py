@@ -286,7 +286,9 @@ def bench_ours(args):
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
     value = ws * T * args.steps / (total_ms / 1e3)
-    launches_per_step = 2 if path in ("auto", "fused") and _fused_available(api, wd, w) else 4
+    fused = path in ("auto", "fused") and _fused_available(api, wd, w)
+    # fused: chunk enumeration, work list, [empty-segment states], fused kernel
+    launches_per_step = (3 + bool(w.want_ht)) if fused else 4
     hbm, tflops, peak_kind = peaks()
     alg_b = algorithmic_bytes(w)
     alg_f = algorithmic_flops(w)
@@ -296,7 +298,7 @@ def bench_ours(args):
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if launches_per_step == 2 else "f32", "data": "synthetic",
+            "dtype": "bf16" if fused else "f32", "data": "synthetic",
             "config": {"workload": w.name, "T": T, "H": H, "Hk": w.Hk, "d": D, "n_seq": N,
                        "n_chunks": w.n_chunks(), "path": path,
                        "l2": "inputs (2.16 GB) exceed the 129 MB L2; no flush between steps",
