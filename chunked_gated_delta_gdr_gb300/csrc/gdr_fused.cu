@@ -54,26 +54,40 @@ constexpr uint32_t kStageBytes = kKQBytes + kVBytes;
 constexpr uint32_t OFF_STAGE = 0;
 constexpr uint32_t OFF_ST = OFF_STAGE + kStages * kStageBytes;  // S^T bf16, 2 key blocks x 128 rows
 constexpr uint32_t OFF_WT = OFF_ST + 32768;                     // W^T bf16, 128 rows (dk) x 64 tok
-constexpr uint32_t OFF_TB = OFF_WT + 16384;                     // Tm diag(beta) bf16, 64 x 64
-constexpr uint32_t OFF_TBG = OFF_TB + 8192;                     // Tm diag(beta e^G) bf16
-constexpr uint32_t OFF_P = OFF_TBG + 8192;                      // P bf16, 64 x 64
-constexpr uint32_t OFF_VT = OFF_P + 8192;                       // V'^T bf16, 128 rows (dv) x 64 tok
-constexpr uint32_t OFF_VS = OFF_VT + 16384;                     // V''^T bf16
-constexpr uint32_t OFF_A = OFF_VS + 16384;                      // solve scratch fp32 64 x 64
-constexpr uint32_t OFF_Y = OFF_A + 16384;                       // solve scratch fp32 32 x 32
-constexpr uint32_t OFF_SMALL = OFF_Y + 4096;
-constexpr uint32_t kSmemBytes = OFF_SMALL + 2048 + 1024;  // + small arrays + alignment slack
+constexpr uint32_t OFF_P = OFF_WT + 16384;                      // P bf16, 2 buffers of 64 x 64
+constexpr uint32_t OFF_VT = OFF_P + 16384;                      // V'^T bf16, 128 rows (dv) x 64 tok
+constexpr uint32_t OFF_VS = OFF_VT + 16384;                     // V''^T bf16; output staging
+constexpr uint32_t OFF_A = OFF_VS + 16384;                      // solve scratch fp32 64 x 65
+constexpr uint32_t OFF_TB = OFF_A;           // Tm diag(beta) bf16 64 x 64, aliases the scratch
+constexpr uint32_t OFF_TBG = OFF_A + 8192;   // Tm diag(beta e^G) bf16, aliases the scratch
+constexpr uint32_t OFF_Y = OFF_A + 17408;    // solve scratch fp32 32 x 40
+constexpr uint32_t OFF_SMALL = OFF_Y + 5120;
+constexpr uint32_t kSmemBytes = OFF_SMALL + 4096 + 1024;  // + small arrays + alignment slack
+constexpr int kLdA = 68, kLdY = 40, kLdX = 24;  // padded leading dims of the fp32 scratch
 
 // ---- TMEM columns ----
 constexpr uint32_t TM_S = 0;     // S^T fp32, 128 columns (key dim)
 constexpr uint32_t TM_X1 = 128;  // [KK^T ; QK^T], 64 columns
 constexpr uint32_t TM_U0 = 192;  // U^T / V'^T, two buffers of 64 columns
 constexpr uint32_t TM_W = 320;   // W^T, 64 columns
-constexpr uint32_t TM_O = 384;   // O^T, 64 columns
+constexpr uint32_t TM_O = 384;   // S^T Q^T (inter-chunk part of O^T), 64 columns
+constexpr uint32_t TM_O2 = 448;  // V'^T P^T (intra-chunk part of O^T), 64 columns
 constexpr uint32_t kTmemCols = 512;
 
 struct UnitInfo {
   int32_t seq, head, t0, end, nch, pad0, pad1, pad2;
+};
+
+// Per-chunk vectors, computed by the producer warp from g and beta.  Three
+// slots (by chunk index) keep a chunk's vectors alive until its output epilogue.
+constexpr int kInfo = 3;
+struct ChunkVec {
+  alignas(16) float G[64];     // chunk-local inclusive cumsum of g, times log2(e)
+  alignas(16) float eG[64];    // exp(G_j)
+  alignas(16) float dec[64];   // exp(G_last - G_j)
+  alignas(16) float beta[64];  // beta (0 past the chunk's end)
+  float eL;                    // exp(G_last)
+  float pad[3];
 };
 
 struct Small {
@@ -82,13 +96,11 @@ struct Small {
       o_full, o_free, drain;
   uint64_t unit_full[kUnitRing], unit_empty[kUnitRing];
   UnitInfo unit[kUnitRing];
-  float gsm[kStages][64];  // g of the chunk (0 past its end)
-  float bsm[kStages][64];  // beta of the chunk (0 past its end)
-  float G[2][64];          // chunk-local inclusive cumsum of g
+  ChunkVec cv[kInfo];
   uint32_t tmem_base;
   int32_t abort;
 };
-static_assert(sizeof(Small) <= 2048, "small area too large");
+static_assert(sizeof(Small) <= 4096, "small area too large");
 
 struct Params {
   int32_t T, n_seq, Hk, H, D, has_h0;
@@ -155,33 +167,17 @@ __device__ __forceinline__ bool wait_wg(Small *sm, uint64_t &bar, uint32_t parit
 }
 constexpr uint32_t kBarPrep = 1, kBarState = 2;
 
-// swizzled index of fp32 element (r, c) in a 64-wide scratch matrix
-__device__ __forceinline__ int aix(int r, int c) { return r * 64 + (c ^ (r & 31)); }
-__device__ __forceinline__ int yix(int r, int c) { return r * 32 + (c ^ (r & 31)); }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
+               "r"(d));
 }
 __device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t &a, uint32_t &b,
                                              uint32_t &c, uint32_t &d) {
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
-               : "r"(addr)
-               : "memory");
-}
-
-// Write 64 fp32 values (as bf16) into row `row` of a 128-byte-swizzled tile whose
-// rows are 64 bf16 wide (one 8 KB / 16 KB block).
-__device__ __forceinline__ void store_row64(uint32_t tile, int row, const float *v) {
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    st_shared_v4(tile + sw128_off(row, q * 8), pack_bf16(v[q * 8 + 0], v[q * 8 + 1]),
-                 pack_bf16(v[q * 8 + 2], v[q * 8 + 3]), pack_bf16(v[q * 8 + 4], v[q * 8 + 5]),
-                 pack_bf16(v[q * 8 + 6], v[q * 8 + 7]));
-  }
+               : "r"(addr));
 }
 
 __device__ __forceinline__ void zero_row(uint32_t tile, int row) {
@@ -237,13 +233,22 @@ __device__ void role_producer(const Params &p, Small *sm, uint8_t *base,
     const int hk = ui.head / (p.H / p.Hk);
     for (int c = 0; c < ui.nch; ++c, ++g) {
       const int s = g % kStages;
+      const int t = ui.t0 + c * kChunk;
+      const int len = min(kChunk, ui.end - t);
+      // g and beta of tokens 2*lane and 2*lane+1 (issued before waiting for the stage)
+      const int j0 = 2 * lane, j1 = 2 * lane + 1;
+      const int64_t r0 = (int64_t)(t + j0), r1 = (int64_t)(t + j1);
+      const float g0 = j0 < len ? p.g[r0 * p.g_st + (int64_t)ui.head * p.g_sh] : 0.f;
+      const float g1 = j1 < len ? p.g[r1 * p.g_st + (int64_t)ui.head * p.g_sh] : 0.f;
+      const float b0 =
+          j0 < len ? __bfloat162float(p.beta[r0 * p.b_st + (int64_t)ui.head * p.b_sh]) : 0.f;
+      const float b1 =
+          j1 < len ? __bfloat162float(p.beta[r1 * p.b_st + (int64_t)ui.head * p.b_sh]) : 0.f;
       if (g >= (uint32_t)kStages &&
           !wait_warp(sm, sm->empty[s], ((g / kStages) - 1) & 1, 0x103)) {
         ok = false;
         break;
       }
-      const int t = ui.t0 + c * kChunk;
-      const int len = min(kChunk, ui.end - t);
       uint8_t *kq = base + OFF_STAGE + s * kStageBytes;
       uint8_t *vv = kq + kKQBytes;
       if (lane == 0) {
@@ -257,16 +262,29 @@ __device__ void role_producer(const Params &p, Small *sm, uint8_t *base,
           tma_load_3d(vv + 8192, mv, &sm->full[s], 64, ui.head, t);
         }
       }
+      {
+        // chunk-local cumsum of g and the decay vectors; the slot (chunk g mod 3) was
+        // last read by chunk g-3's output epilogue, which precedes the stage release
+        ChunkVec &cv = sm->cv[g % kInfo];
+        float sum = g0 + g1;
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int j = lane + 32 * r;
-        float gv = 0.f, bv = 0.f;
-        if (j < len) {
-          gv = p.g[(int64_t)(t + j) * p.g_st + (int64_t)ui.head * p.g_sh];
-          bv = __bfloat162float(p.beta[(int64_t)(t + j) * p.b_st + (int64_t)ui.head * p.b_sh]);
+        for (int off = 1; off < 32; off <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, sum, off);
+          if (lane >= off) sum += y;
         }
-        sm->gsm[s][j] = gv;
-        sm->bsm[s][j] = bv;
+        // decay factors e^x are evaluated as 2^(x log2 e) on the special-function unit
+        constexpr float kLog2e = 1.4426950408889634f;
+        const float G0 = (sum - g1) * kLog2e, G1 = sum * kLog2e;
+        const float GL = __shfl_sync(0xffffffffu, G1, 31);
+        cv.G[j0] = G0;
+        cv.G[j1] = G1;
+        cv.eG[j0] = ex2(G0);
+        cv.eG[j1] = ex2(G1);
+        cv.dec[j0] = ex2(GL - G0);
+        cv.dec[j1] = ex2(GL - G1);
+        cv.beta[j0] = b0;
+        cv.beta[j1] = b1;
+        if (lane == 0) cv.eL = ex2(GL);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm->full[s]);
@@ -330,13 +348,18 @@ __device__ void role_mma(const Params &p, Small *sm, uint8_t *base) {
                  sdesc_sw128(sbase + OFF_TBG + kk * 32, 0, 1024), id_uw, kk > 0);
       }
       mma_commit(&sm->uw_full);
-      // next chunk's X1 (prep of c+1 overlaps this chunk's scan)
-      if (c + 1 < ui.nch) {
-        if (!wait1(sm, sm->full[(g + 1) % kStages], ((g + 1) / kStages) & 1, 0x205)) { ok = false; break; }
-        if (!wait1(sm, sm->x1_free, g & 1, 0x206)) { ok = false; break; }
-        tc_fence_after();
-        issue_x1(g + 1);
-      }
+      // next chunk's X1 (prep of c+1 overlaps this chunk's scan): issued as soon as
+      // its stage has landed, without holding up this chunk's scan MMAs
+      bool x1_pending = c + 1 < ui.nch;
+      const uint32_t s1 = (g + 1) % kStages, ph1 = ((g + 1) / kStages) & 1;
+      auto try_x1 = [&]() {
+        if (x1_pending && mbar_test(&sm->full[s1], ph1) && mbar_test(&sm->x1_free, g & 1)) {
+          tc_fence_after();
+          issue_x1(g + 1);
+          x1_pending = false;
+        }
+      };
+      try_x1();
       // V'^T = U^T - S^T W^T
       if (!wait1(sm, sm->s_ready, g & 1, 0x207)) { ok = false; break; }
       if (!wait1(sm, sm->wt_ready, g & 1, 0x208)) { ok = false; break; }
@@ -347,6 +370,7 @@ __device__ void role_mma(const Params &p, Small *sm, uint8_t *base) {
                  sdesc_sw128(sbase + OFF_WT + kk * 2048, 16384, 1024), id_vp, 1);
       }
       mma_commit(&sm->vp_full);
+      try_x1();
       // O^T = S^T Q~^T
       if (g >= 1 && !wait1(sm, sm->o_free, (g - 1) & 1, 0x209)) { ok = false; break; }
       tc_fence_after();
@@ -357,6 +381,7 @@ __device__ void role_mma(const Params &p, Small *sm, uint8_t *base) {
                  sdesc_sw128(kq + (kk / 4) * 16384 + 8192 + (kk % 4) * 32, 0, 1024), id_o1,
                  kk > 0);
       }
+      try_x1();
       // S^T += V''^T K ;  O^T += V'^T P^T
       if (!wait1(sm, sm->vp_ready, g & 1, 0x20a)) { ok = false; break; }
       tc_fence_after();
@@ -368,11 +393,17 @@ __device__ void role_mma(const Params &p, Small *sm, uint8_t *base) {
       mma_commit(&sm->s_full);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        mma_bf16(tb + TM_O, sdesc_sw128(sbase + OFF_VT + kk * 32, 0, 1024),
-                 sdesc_sw128(sbase + OFF_P + kk * 32, 0, 1024), id_o2, 1);
+        mma_bf16(tb + TM_O2, sdesc_sw128(sbase + OFF_VT + kk * 32, 0, 1024),
+                 sdesc_sw128(sbase + OFF_P + (g & 1) * 8192 + kk * 32, 0, 1024), id_o2, kk > 0);
       }
       mma_commit(&sm->o_full);
       mma_commit(&sm->empty[s]);
+      if (x1_pending) {
+        if (!wait1(sm, sm->full[s1], ph1, 0x205)) { ok = false; break; }
+        if (!wait1(sm, sm->x1_free, g & 1, 0x206)) { ok = false; break; }
+        tc_fence_after();
+        issue_x1(g + 1);
+      }
     }
   }
   // drain: every MMA issued so far must finish before TMEM is released
@@ -380,19 +411,72 @@ __device__ void role_mma(const Params &p, Small *sm, uint8_t *base) {
   mbar_wait(&sm->drain, 0, nullptr, kWaitLimitNs);
 }
 
+// Pack eight fp32 values as bf16 into one 16-byte chunk of a swizzled tile row.
+__device__ __forceinline__ void store_chunk8(uint32_t tile, int row, int col, const float *v) {
+  st_shared_v4(tile + sw128_off(row, col), pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]),
+               pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
+}
+
+__device__ __forceinline__ void ld_f4(const float *p, float *v) {
+  const float4 x = *reinterpret_cast<const float4 *>(p);
+  v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+}
+__device__ __forceinline__ void st_f4(float *p, const float *v) {
+  *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
+// One warp: c[16 x 16] += A[16 x K] * B[K x 16] on the tensor pipe (tf32 in, fp32
+// accumulate, mma.sync m16n8k8); A and B are fp32 row-major in shared memory.
+__device__ __forceinline__ void warp_mm16(const float *A, int lda, const float *B, int ldb,
+                                          int K, float (&c)[2][4]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  for (int k = 0; k < K; k += 8) {
+    const uint32_t a0 = to_tf32(A[g * lda + k + t]), a1 = to_tf32(A[(g + 8) * lda + k + t]);
+    const uint32_t a2 = to_tf32(A[g * lda + k + t + 4]), a3 = to_tf32(A[(g + 8) * lda + k + t + 4]);
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+      const uint32_t b0 = to_tf32(B[(k + t) * ldb + n * 8 + g]);
+      const uint32_t b1 = to_tf32(B[(k + t + 4) * ldb + n * 8 + g]);
+      asm volatile(
+          "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+          "{%8,%9}, {%0,%1,%2,%3};"
+          : "+f"(c[n][0]), "+f"(c[n][1]), "+f"(c[n][2]), "+f"(c[n][3])
+          : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+  }
+}
+
+__device__ __forceinline__ void warp_store16(float *C, int ldc, const float (&c)[2][4], float s) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int n = 0; n < 2; ++n) {
+    C[g * ldc + n * 8 + 2 * t] = s * c[n][0];
+    C[g * ldc + n * 8 + 2 * t + 1] = s * c[n][1];
+    C[(g + 8) * ldc + n * 8 + 2 * t] = s * c[n][2];
+    C[(g + 8) * ldc + n * 8 + 2 * t + 1] = s * c[n][3];
+  }
+}
+
 // The prep warpgroup.  `row` is this thread's TMEM lane (0..127).
 __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
   const uint32_t tb = sm->tmem_base;
   const uint32_t sbase = smem_u32(base);
   const uint32_t lane_base = (uint32_t)(row & ~31);
-  float *Asc = reinterpret_cast<float *>(base + OFF_A);
-  float *Ysc = reinterpret_cast<float *>(base + OFF_Y);
-  const int pid = row;  // 0..127, unique in the warpgroup
+  float *AS = reinterpret_cast<float *>(base + OFF_A);  // 64 x kLdA fp32
+  float *YS = reinterpret_cast<float *>(base + OFF_Y);  // 32 x kLdY fp32 (also 2 x 16 x kLdX)
+  const int pid = row;           // 0..127, unique in the warpgroup
+  const int wq = pid >> 5;       // warp index by lane quadrant
   uint32_t g = 0;
   bool ok = true;
   for (uint32_t k = 0; ok; ++k) {
     const int slot = k % kUnitRing;
-    if (!wait_wg(sm, sm->unit_full[slot], (k / kUnitRing) & 1, 0x301, kBarPrep)) { ok = false; break; }
+    if (!wait_wg(sm, sm->unit_full[slot], (k / kUnitRing) & 1, 0x301, kBarPrep)) break;
     const UnitInfo ui = sm->unit[slot];
     mbar_arrive(&sm->unit_empty[slot]);
     if (ui.seq < 0) break;
@@ -400,8 +484,8 @@ __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
       const uint32_t s = g % kStages;
       const int t = ui.t0 + c * kChunk;
       const int len = min(kChunk, ui.end - t);
-      uint8_t *kq = base + OFF_STAGE + s * kStageBytes;
-      const uint32_t kq_a = smem_u32(kq);
+      const uint32_t kq_a = sbase + OFF_STAGE + s * kStageBytes;
+      const int cb2 = g & 1;
       if (!wait_wg(sm, sm->full[s], (g / kStages) & 1, 0x302, kBarPrep)) { ok = false; break; }
       // zero the rows past the chunk's end (they hold the next segment's tokens)
       if (len < kChunk) {
@@ -417,170 +501,129 @@ __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
         }
         fence_async_smem();
       }
-      float *Gc = sm->G[g & 1];
-      if (pid < 32) {  // chunk-local inclusive cumsum, two tokens per lane
-        const float a = sm->gsm[s][2 * pid], b = sm->gsm[s][2 * pid + 1];
-        float sum = a + b;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const float y = __shfl_up_sync(0xffffffffu, sum, off);
-          if (pid >= off) sum += y;
-        }
-        const float ex = sum - (a + b);
-        Gc[2 * pid] = ex + a;
-        Gc[2 * pid + 1] = ex + a + b;
-      }
-      named_bar(1, 128);
+      const ChunkVec &cv = sm->cv[g % kInfo];
       // X1 rows: lanes 0-63 = K K^T (rows of A), lanes 64-127 = Q K^T (rows of P)
       if (!wait_wg(sm, sm->x1_full, g & 1, 0x303, kBarPrep)) { ok = false; break; }
       tc_fence_after();
-      float xr[64];
       {
-        uint32_t r0[32], r1[32];
-        tmem_ld32(tmem_addr(tb + TM_X1, lane_base, 0), r0);
-        tmem_ld32(tmem_addr(tb + TM_X1, lane_base, 32), r1);
-        tmem_ld_wait();
+        const int i = row & 63;
+        const float *Gc = cv.G;
+        const float gi = Gc[i];
+        const bool live = i < len;
+        const float scl = (row < 64) ? cv.beta[i] : 1.f;
+#pragma unroll 1
+        for (int h = 0; h < 4; ++h) {  // 16 columns at a time
+          uint32_t r[16];
+          tmem_ld16(tmem_addr(tb + TM_X1, lane_base, h * 16), r);
+          float gv[16];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          xr[j] = __uint_as_float(r0[j]);
-          xr[j + 32] = __uint_as_float(r1[j]);
+          for (int q = 0; q < 4; ++q) ld_f4(Gc + h * 16 + q * 4, gv + q * 4);
+          tmem_ld_wait();
+          const int lim = (row < 64) ? i : i + 1;  // A: j < i, P: j <= i
+          float v[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const int j = h * 16 + u;
+            const float e = ex2(gi - gv[u]);
+            const float prod = scl * e * __uint_as_float(r[u]);
+            v[u] = (live && j < lim) ? prod : 0.f;
+          }
+          if (row < 64) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) st_f4(AS + i * kLdA + h * 16 + q * 4, v + q * 4);
+          } else {
+            const uint32_t ptile = sbase + OFF_P + cb2 * 8192;
+            store_chunk8(ptile, i, h * 16, v);
+            store_chunk8(ptile, i, h * 16 + 8, v + 8);
+          }
         }
       }
       tc_fence_before();
       mbar_arrive(&sm->x1_free);
-      uint32_t pk[32];  // packed P row (bf16x2), rows 64..127 only
-      if (row < 64) {
-        const int i = row;
-        const float bi = sm->bsm[s][i], gi = Gc[i];
+      named_bar(kBarPrep, 128);
+      // ---- Tm = (I + A)^-1, 64 x 64 unit lower triangular, fp32 ----
+      // phase 1: the four 16 x 16 diagonal blocks by forward substitution, one
+      // column per thread (threads 0..63)
+      {
+        const int b = (pid >> 4) & 3, cc = pid & 15;
+        float *blk = AS + 16 * b * kLdA + 16 * b;
+        float x[16];
+        if (pid < 64) {
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const float a = (j < i && i < len) ? bi * __expf(gi - Gc[j]) * xr[j] : 0.f;
-          Asc[aix(i, j)] = a;
-        }
-      } else {
-        const int i = row - 64;
-        const float gi = Gc[i];
+          for (int r = 0; r < 16; ++r) {
+            float a[16];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int j0 = 2 * j, j1 = 2 * j + 1;
-          const float p0 = (j0 <= i && i < len) ? __expf(gi - Gc[j0]) * xr[j0] : 0.f;
-          const float p1 = (j1 <= i && i < len) ? __expf(gi - Gc[j1]) * xr[j1] : 0.f;
-          pk[j] = pack_bf16(p0, p1);
-        }
-        // Q~ row i = e^{G_i} q_i (in place in the stage; rows past len are zero)
-        if (i < len) {
-          const float e = __expf(gi);
+            for (int q = 0; q < 4; ++q) ld_f4(blk + r * kLdA + q * 4, a + q * 4);
+            float s0 = (r == cc) ? 1.f : 0.f, s1 = 0.f;
 #pragma unroll
-          for (int kb = 0; kb < 2; ++kb) {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const uint32_t addr = kq_a + kb * 16384 + sw128_off(64 + i, q * 8);
-              uint32_t w0, w1, w2, w3;
-              ld_shared_v4(addr, w0, w1, w2, w3);
-              st_shared_v4(addr, pack_bf16(bf_lo(w0) * e, bf_hi(w0) * e),
-                           pack_bf16(bf_lo(w1) * e, bf_hi(w1) * e),
-                           pack_bf16(bf_lo(w2) * e, bf_hi(w2) * e),
-                           pack_bf16(bf_lo(w3) * e, bf_hi(w3) * e));
+            for (int m = 0; m < r; ++m) {
+              if (m & 1) s1 -= a[m] * x[m]; else s0 -= a[m] * x[m];
             }
+            x[r] = s0 + s1;
           }
         }
-      }
-      named_bar(1, 128);
-      // ---- Tm = (I + A)^-1, 64 x 64 unit lower triangular, fp32 ----
-      // phase 1: the four 16 x 16 diagonal blocks, one column per thread
-      float x[16];
-      if (pid < 64) {
-        const int b = pid >> 4, cc = pid & 15, o = 16 * b;
+        named_bar(kBarPrep, 128);
+        if (pid < 64) {
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          float v = (r == cc) ? 1.f : 0.f;
-#pragma unroll
-          for (int m = 0; m < r; ++m) v -= Asc[aix(o + r, o + m)] * x[m];
-          x[r] = v;
+          for (int r = 0; r < 16; ++r) blk[r * kLdA + cc] = x[r];
         }
       }
-      named_bar(1, 128);
-      if (pid < 64) {
-        const int b = pid >> 4, cc = pid & 15, o = 16 * b;
-#pragma unroll
-        for (int r = 0; r < 16; ++r) Asc[aix(o + r, o + cc)] = x[r];
-      }
-      named_bar(1, 128);
-      // phase 2: T_{b+1,b} = -D_{b+1} A_{b+1,b} D_b for b = 0, 2
+      named_bar(kBarPrep, 128);
+      // phase 2: T_{b+1,b} = -D_{b+1} A_{b+1,b} D_b for b = 0, 2 (warps 0 and 1)
       {
-        const int blk = pid >> 6, q = pid & 63, r = q >> 2, c0 = (q & 3) * 4;
-        const int ob = 32 * blk, oa = ob + 16;  // D_b at ob, the block below at oa
-        float xv[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          const float a = Asc[aix(oa + r, ob + m)];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) xv[u] += a * Asc[aix(ob + m, ob + c0 + u)];
+        float *X = YS + wq * 16 * kLdX;
+        const int ob = 32 * wq, oa = ob + 16;
+        if (wq < 2) {
+          float acc[2][4] = {};
+          warp_mm16(AS + oa * kLdA + ob, kLdA, AS + ob * kLdA + ob, kLdA, 16, acc);
+          warp_store16(X, kLdX, acc, 1.f);
         }
-        named_bar(1, 128);
-        float *Xs = Ysc + blk * 256;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) Xs[r * 16 + ((c0 + u) ^ r)] = xv[u];
-        named_bar(1, 128);
-        float tv[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          const float d = Asc[aix(oa + r, oa + m)];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) tv[u] -= d * Xs[m * 16 + ((c0 + u) ^ m)];
+        named_bar(kBarPrep, 128);
+        if (wq < 2) {
+          float acc[2][4] = {};
+          warp_mm16(AS + oa * kLdA + oa, kLdA, X, kLdX, 16, acc);
+          warp_store16(AS + oa * kLdA + ob, kLdA, acc, -1.f);
         }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) Asc[aix(oa + r, ob + c0 + u)] = tv[u];
       }
-      named_bar(1, 128);
-      // phase 3: Tm[32:64, 0:32] = -T2 (A[32:64, 0:32] T1)
+      named_bar(kBarPrep, 128);
+      // phase 3: Tm[32:64, 0:32] = -T2 (A[32:64, 0:32] T1), one 16 x 16 tile per warp
       {
-        const int r = pid >> 2, c0 = (pid & 3) * 8;
-        float yv[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) yv[u] = 0.f;
-        for (int m = c0; m < 32; ++m) {
-          const float a = Asc[aix(32 + r, m)];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) yv[u] += a * Asc[aix(m, c0 + u)];
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) Ysc[yix(r, c0 + u)] = yv[u];
-        named_bar(1, 128);
-        float tv[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) tv[u] = 0.f;
-        for (int m = 0; m <= r; ++m) {
-          const float d = Asc[aix(32 + r, 32 + m)];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) tv[u] -= d * Ysc[yix(m, c0 + u)];
-        }
-        named_bar(1, 128);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) Asc[aix(32 + r, c0 + u)] = tv[u];
+        const int mt = wq >> 1, nt = wq & 1;
+        float acc[2][4] = {};
+        warp_mm16(AS + (32 + 16 * mt) * kLdA, kLdA, AS + 16 * nt, kLdA, 32, acc);
+        warp_store16(YS + 16 * mt * kLdY + 16 * nt, kLdY, acc, 1.f);
+        named_bar(kBarPrep, 128);
+        float acc2[2][4] = {};
+        warp_mm16(AS + (32 + 16 * mt) * kLdA + 32, kLdA, YS + 16 * nt, kLdY, 32, acc2);
+        named_bar(kBarPrep, 128);
+        warp_store16(AS + (32 + 16 * mt) * kLdA + 16 * nt, kLdA, acc2, -1.f);
       }
-      named_bar(1, 128);
-      // Tm diag(beta) and Tm diag(beta e^G) as bf16 MMA operands (row i = thread i)
-      if (row < 64) {
-        const int i = row;
-        float v[64];
+      named_bar(kBarPrep, 128);
+      // Tm diag(beta) and Tm diag(beta e^G) as bf16 operands, half a row per thread;
+      // they overwrite the scratch, so every row is read before any is written
+      {
+        const int ri = pid & 63, hc = (pid >> 6) * 32;
+        float v[32];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) v[j] = (j <= i) ? Asc[aix(i, j)] * sm->bsm[s][j] : 0.f;
-        store_row64(sbase + OFF_TB, i, v);
+        for (int q = 0; q < 8; ++q) {
+          float tq[4], bq[4];
+          ld_f4(AS + ri * kLdA + hc + q * 4, tq);
+          ld_f4(cv.beta + hc + q * 4, bq);
 #pragma unroll
-        for (int j = 0; j < 64; ++j) v[j] *= __expf(Gc[j]);
-        store_row64(sbase + OFF_TBG, i, v);
-      }
-      // P waits until the previous chunk's output MMA has read the buffer
-      if (g >= 1 && !wait_wg(sm, sm->o_full, (g - 1) & 1, 0x304, kBarPrep)) { ok = false; break; }
-      if (row >= 64) {
-        {
-          const int i = row - 64;
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            st_shared_v4(sbase + OFF_P + sw128_off(i, q * 8), pk[4 * q], pk[4 * q + 1],
-                         pk[4 * q + 2], pk[4 * q + 3]);
+          for (int u = 0; u < 4; ++u) v[q * 4 + u] = (hc + q * 4 + u <= ri) ? tq[u] * bq[u] : 0.f;
         }
+        named_bar(kBarPrep, 128);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) store_chunk8(sbase + OFF_TB, ri, hc + q * 8, v + q * 8);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float eq[4];
+          ld_f4(cv.eG + hc + q * 4, eq);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) v[q * 4 + u] *= eq[u];
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) store_chunk8(sbase + OFF_TBG, ri, hc + q * 8, v + q * 8);
       }
       fence_async_smem();
       mbar_arrive(&sm->t_ready);
@@ -593,13 +636,13 @@ __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
         tmem_ld32(tmem_addr(tb + TM_W, lane_base, 0), r0);
         tmem_ld32(tmem_addr(tb + TM_W, lane_base, 32), r1);
         tmem_ld_wait();
-        float v[64];
+        float v[8];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          v[j] = __uint_as_float(r0[j]);
-          v[j + 32] = __uint_as_float(r1[j]);
+        for (int q = 0; q < 8; ++q) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) v[u] = __uint_as_float(q < 4 ? r0[q * 8 + u] : r1[(q - 4) * 8 + u]);
+          store_chunk8(sbase + OFF_WT, row, q * 8, v);
         }
-        store_row64(sbase + OFF_WT, row, v);
       }
       fence_async_smem();
       tc_fence_before();
@@ -615,98 +658,123 @@ __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
   const uint32_t lane_base = (uint32_t)(row & ~31);
   const int dv = row;
   const int D = p.D;
+  uint8_t *stage_o = base + OFF_VS;  // output staging [64 tokens][128 dv] bf16
   uint32_t g = 0;
   bool ok = true;
   int prev_t = 0, prev_len = 0, prev_head = 0;
   auto epilogue = [&](uint32_t gg) -> bool {
     if (!wait_wg(sm, sm->o_full, gg & 1, 0x401, kBarState)) return false;
     tc_fence_after();
-    uint32_t r0[32], r1[32];
-    tmem_ld32(tmem_addr(tb + TM_O, lane_base, 0), r0);
-    tmem_ld32(tmem_addr(tb + TM_O, lane_base, 32), r1);
-    tmem_ld_wait();
-    tc_fence_before();
-    mbar_arrive(&sm->o_free);
-    if (dv < D) {
-      __nv_bfloat16 *op = p.o + (int64_t)prev_head * p.o_sh + dv;
+    const float *eG = sm->cv[gg % kInfo].eG;
+    __nv_bfloat16 *st = reinterpret_cast<__nv_bfloat16 *>(stage_o) + dv;
+#pragma unroll 1
+    for (int hb = 0; hb < 2; ++hb) {  // O = scale (e^{G_i} (S^T Q^T)_i + (V'^T P^T)_i)
+      uint32_t r1[32], r2[32];
+      tmem_ld32(tmem_addr(tb + TM_O, lane_base, hb * 32), r1);
+      tmem_ld32(tmem_addr(tb + TM_O2, lane_base, hb * 32), r2);
+      float e[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i < prev_len)
-          op[(int64_t)(prev_t + i) * p.o_st] = __float2bfloat16_rn(p.scale * __uint_as_float(r0[i]));
+      for (int q = 0; q < 8; ++q) ld_f4(eG + hb * 32 + q * 4, e + q * 4);
+      tmem_ld_wait();
+      if (hb == 1) {
+        tc_fence_before();
+        mbar_arrive(&sm->o_free);
+      }
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i + 32 < prev_len)
-          op[(int64_t)(prev_t + 32 + i) * p.o_st] =
-              __float2bfloat16_rn(p.scale * __uint_as_float(r1[i]));
+      for (int u = 0; u < 32; ++u)
+        st[(hb * 32 + u) * 128] = __float2bfloat16_rn(
+            p.scale * fmaf(e[u], __uint_as_float(r1[u]), __uint_as_float(r2[u])));
+    }
+    named_bar(kBarState, 128);
+    const int chunks_per_row = D / 8;
+#pragma unroll 2
+    for (int idx = row; idx < prev_len * 16; idx += 128) {
+      const int i = idx >> 4, ch = idx & 15;
+      if (ch < chunks_per_row) {
+        const uint4 val = *reinterpret_cast<const uint4 *>(stage_o + i * 256 + ch * 16);
+        *reinterpret_cast<uint4 *>(p.o + (int64_t)(prev_t + i) * p.o_st +
+                                   (int64_t)prev_head * p.o_sh + ch * 8) = val;
+      }
     }
     return true;
   };
   for (uint32_t k = 0; ok; ++k) {
     const int slot = k % kUnitRing;
-    if (!wait_wg(sm, sm->unit_full[slot], (k / kUnitRing) & 1, 0x402, kBarState)) { ok = false; break; }
+    if (!wait_wg(sm, sm->unit_full[slot], (k / kUnitRing) & 1, 0x402, kBarState)) break;
     const UnitInfo ui = sm->unit[slot];
     mbar_arrive(&sm->unit_empty[slot]);
     if (ui.seq < 0) break;
-    const int64_t sbase_idx = ((int64_t)ui.seq * p.H + ui.head) * D * D;
+    const int64_t sidx = ((int64_t)ui.seq * p.H + ui.head) * D * D;
     for (int c = 0; c < ui.nch; ++c, ++g) {
       const int t = ui.t0 + c * kChunk;
       const int len = min(kChunk, ui.end - t);
+      const int cb2 = g & 1;
       if (!wait_wg(sm, sm->t_ready, g & 1, 0x403, kBarState)) { ok = false; break; }
-      const float *Gc = sm->G[g & 1];
-      const float GL = Gc[len - 1];
-      const float eL = __expf(GL);
-      // current state row dv of S^T: from h0 at a unit's first chunk, else from TMEM
-      float sr[128];
-      if (c == 0) {
-#pragma unroll
-        for (int j = 0; j < 128; ++j)
-          sr[j] = (p.has_h0 && dv < D && j < D) ? p.h0[sbase_idx + (int64_t)j * D + dv] : 0.f;
-      } else {
+      const float eL = sm->cv[g % kInfo].eL;
+      if (c >= 1) {
         if (!wait_wg(sm, sm->s_full, (g - 1) & 1, 0x404, kBarState)) { ok = false; break; }
         tc_fence_after();
-#pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
-          uint32_t r[32];
-          tmem_ld32(tmem_addr(tb + TM_S, lane_base, cb * 32), r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) sr[cb * 32 + j] = __uint_as_float(r[j]);
-        }
       }
-      store_row64(sbase + OFF_ST, row, sr);
-      store_row64(sbase + OFF_ST + 16384, row, sr + 64);
+      // row dv of S^T -> bf16 operand; e^{G_last} S^T back into TMEM
+#pragma unroll 1
+      for (int hb = 0; hb < 2; ++hb) {  // 64 key columns at a time
+        uint32_t r0[32], r1[32];
+        if (c == 0) {
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb) {
-        uint32_t r[32];
+          for (int u = 0; u < 32; ++u) {
+            const int j0 = hb * 64 + u, j1 = hb * 64 + 32 + u;
+            const bool in = p.has_h0 && dv < D;
+            r0[u] = __float_as_uint((in && j0 < D) ? p.h0[sidx + (int64_t)j0 * D + dv] : 0.f);
+            r1[u] = __float_as_uint((in && j1 < D) ? p.h0[sidx + (int64_t)j1 * D + dv] : 0.f);
+          }
+        } else {
+          tmem_ld32(tmem_addr(tb + TM_S, lane_base, hb * 64), r0);
+          tmem_ld32(tmem_addr(tb + TM_S, lane_base, hb * 64 + 32), r1);
+          tmem_ld_wait();
+        }
+        const uint32_t tile = sbase + OFF_ST + hb * 16384;
+        float v[8];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(sr[cb * 32 + j] * eL);
-        tmem_st32(tmem_addr(tb + TM_S, lane_base, cb * 32), r);
+        for (int q = 0; q < 8; ++q) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) v[u] = __uint_as_float(q < 4 ? r0[q * 8 + u] : r1[(q - 4) * 8 + u]);
+          store_chunk8(tile, dv, q * 8, v);
+        }
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+          r0[u] = __float_as_uint(__uint_as_float(r0[u]) * eL);
+          r1[u] = __float_as_uint(__uint_as_float(r1[u]) * eL);
+        }
+        tmem_st32(tmem_addr(tb + TM_S, lane_base, hb * 64), r0);
+        tmem_st32(tmem_addr(tb + TM_S, lane_base, hb * 64 + 32), r1);
       }
       tmem_st_wait();
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&sm->s_ready);
       // previous chunk's output (same unit) while this chunk's V'^T is computed
-      if (c >= 1) {
-        if (!epilogue(g - 1)) { ok = false; break; }
-      }
+      if (c >= 1 && !epilogue(g - 1)) { ok = false; break; }
       if (!wait_wg(sm, sm->vp_full, g & 1, 0x405, kBarState)) { ok = false; break; }
       tc_fence_after();
       {
         uint32_t r0[32], r1[32];
-        tmem_ld32(tmem_addr(tb + TM_U0 + (g & 1) * 64, lane_base, 0), r0);
-        tmem_ld32(tmem_addr(tb + TM_U0 + (g & 1) * 64, lane_base, 32), r1);
+        const uint32_t tu = tb + TM_U0 + (g & 1) * 64;
+        tmem_ld32(tmem_addr(tu, lane_base, 0), r0);
+        tmem_ld32(tmem_addr(tu, lane_base, 32), r1);
+        const float *dec = sm->cv[g % kInfo].dec;
         tmem_ld_wait();
-        float v[64];
+        float v[8], d[8];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          v[j] = __uint_as_float(r0[j]);
-          v[j + 32] = __uint_as_float(r1[j]);
+        for (int q = 0; q < 8; ++q) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) v[u] = __uint_as_float(q < 4 ? r0[q * 8 + u] : r1[(q - 4) * 8 + u]);
+          store_chunk8(sbase + OFF_VT, dv, q * 8, v);
+          ld_f4(dec + q * 8, d);
+          ld_f4(dec + q * 8 + 4, d + 4);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) v[u] *= d[u];
+          store_chunk8(sbase + OFF_VS, dv, q * 8, v);
         }
-        store_row64(sbase + OFF_VT, row, v);
-#pragma unroll
-        for (int j = 0; j < 64; ++j) v[j] *= __expf(GL - Gc[j]);
-        store_row64(sbase + OFF_VS, row, v);
       }
       fence_async_smem();
       tc_fence_before();
@@ -717,25 +785,22 @@ __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
     }
     if (!ok) break;
     // end of the unit: final state, then the last chunk's output
-    if (ui.nch > 0) {
-      if (!wait_wg(sm, sm->s_full, (g - 1) & 1, 0x406, kBarState)) { ok = false; break; }
-      tc_fence_after();
-      if (p.ht) {
+    if (!wait_wg(sm, sm->s_full, (g - 1) & 1, 0x406, kBarState)) break;
+    tc_fence_after();
+    if (p.ht) {
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t r[32];
+        tmem_ld32(tmem_addr(tb + TM_S, lane_base, cb * 32), r);
+        tmem_ld_wait();
+        if (dv < D) {
 #pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
-          uint32_t r[32];
-          tmem_ld32(tmem_addr(tb + TM_S, lane_base, cb * 32), r);
-          tmem_ld_wait();
-          if (dv < D) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (cb * 32 + j < D)
-                p.ht[sbase_idx + (int64_t)(cb * 32 + j) * D + dv] = __uint_as_float(r[j]);
-          }
+          for (int u = 0; u < 32; ++u)
+            if (cb * 32 + u < D) p.ht[sidx + (int64_t)(cb * 32 + u) * D + dv] = __uint_as_float(r[u]);
         }
       }
-      if (!epilogue(g - 1)) { ok = false; break; }
     }
+    if (!epilogue(g - 1)) break;
   }
 }
 
@@ -812,32 +877,62 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Work list: non-empty segments ordered longest first (bucketed by log2 of the
-// chunk count; the order inside a bucket only affects scheduling, never results).
+// Work list: non-empty segments ordered longest first by a counting sort on the
+// chunk count (exact below 4096 chunks; longer segments share the top bucket).
+// The order among equal counts only affects scheduling, never results.
+constexpr int kSortBuckets = 4096;
 __global__ void __launch_bounds__(1024)
     k_worklist(const SegInfo *__restrict__ seg, int32_t n_seq, int32_t *order,
                int32_t *n_active, int32_t *counter) {
-  __shared__ int cnt[33], cur[33];
-  if (threadIdx.x < 33) cnt[threadIdx.x] = 0;
+  __shared__ int cnt[kSortBuckets];
+  __shared__ int warp_sum[32];
+  for (int b = threadIdx.x; b < kSortBuckets; b += blockDim.x) cnt[b] = 0;
   __syncthreads();
   for (int i = threadIdx.x; i < n_seq; i += blockDim.x) {
     const int nc = seg[i].n_chunks;
-    if (nc > 0) atomicAdd(&cnt[31 - __clz(nc)], 1);
+    if (nc > 0) atomicAdd(&cnt[min(nc, kSortBuckets - 1)], 1);
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int b = 31; b >= 0; --b) {
-      cur[b] = acc;
-      acc += cnt[b];
+  // exclusive scan from the largest bucket down: 4 buckets per thread
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  int v[4], tot = 0;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    v[u] = cnt[kSortBuckets - 1 - (4 * t + u)];
+    tot += v[u];
+  }
+  int incl = tot;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_sum[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += y;
     }
-    *n_active = acc;
+    warp_sum[lane] = w;
+  }
+  __syncthreads();
+  int run = incl - tot + (warp > 0 ? warp_sum[warp - 1] : 0);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    cnt[kSortBuckets - 1 - (4 * t + u)] = run;
+    run += v[u];
+  }
+  if (t == 0) {
+    *n_active = warp_sum[31];
     *counter = 0;
   }
   __syncthreads();
   for (int i = threadIdx.x; i < n_seq; i += blockDim.x) {
     const int nc = seg[i].n_chunks;
-    if (nc > 0) order[atomicAdd(&cur[31 - __clz(nc)], 1)] = i;
+    if (nc > 0) order[atomicAdd(&cnt[min(nc, kSortBuckets - 1)], 1)] = i;
   }
 }
 
@@ -889,6 +984,7 @@ bool fused_supported(const FusedArgs &a) {
     if ((a.q_st % 8) || (a.q_sh % 8) || (a.k_st % 8) || (a.k_sh % 8) || (a.v_st % 8) ||
         (a.v_sh % 8))
       return false;
+    if (!al16(a.o) || (a.o_st % 8) || (a.o_sh % 8)) return false;
   }
   return true;
 }
