@@ -184,6 +184,21 @@ def cpu_oracle_sample(w, target_s: float):
                       f"{nh}/{w.H}"}
 
 
+def max_over_ranks(x: float, dist, device="cpu") -> float:
+    """The slowest rank's value (timings are reported as the max over ranks)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_rank: int, steps: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank processes its own copy of the workload."""
+    return world * tokens_per_rank * steps / (max_ms / 1e3)
+
+
 def dist_setup(args):
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -279,13 +294,9 @@ def bench_ours(args):
         dist.barrier()
     clocks = sampler.stop()
     per = [a.elapsed_time(b) for a, b in ev]  # ms, each step on the launching stream
-    total_ms = sum(per)
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(per), dist, dev)
     ms_per_step = total_ms / args.steps
-    value = ws * T * args.steps / (total_ms / 1e3)
+    value = job_tokens_per_s(ws, T, args.steps, total_ms)
     fused = path in ("auto", "fused") and _fused_available(api, wd, w)
     # fused: chunk enumeration, work list, [empty-segment states], fused kernel
     launches_per_step = (3 + bool(w.want_ht)) if fused else 4
@@ -301,7 +312,8 @@ def bench_ours(args):
             "dtype": "bf16" if fused else "f32", "data": "synthetic",
             "config": {"workload": w.name, "T": T, "H": H, "Hk": w.Hk, "d": D, "n_seq": N,
                        "n_chunks": w.n_chunks(), "path": path,
-                       "l2": "inputs (2.16 GB) exceed the 129 MB L2; no flush between steps",
+                       "l2": (f"inputs ({alg_b / 1e9:.2f} GB) exceed the 129 MB L2; "
+                              "no flush between steps"),
                        "per_rank": "each rank runs its own copy of the workload"},
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
                          "frac": achieved_gbs / hbm, "peak_kind": f"{peak_kind} burst copy",
@@ -361,11 +373,7 @@ def bench_e2e(args, api, w, dev, path, dist):
     for _ in range(steps):
         step()
     torch.cuda.synchronize()
-    el = time.perf_counter() - t0
-    if dist is not None:
-        t = torch.tensor([el], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        el = float(t.item())
+    el = max_over_ranks(time.perf_counter() - t0, dist, dev)
     ws = dist.get_world_size() if dist is not None else 1
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg, hb, hh0, w.cu_seqlens)
               if t is not None)

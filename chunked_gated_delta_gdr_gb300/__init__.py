@@ -16,6 +16,7 @@ from .api import (  # noqa: F401
     device_status,
     stage_workspace_bytes,
     state_scan,
+    wait_selftest,
     workspace_bytes,
 )
 from ._native import GdrError  # noqa: F401

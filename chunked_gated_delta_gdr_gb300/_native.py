@@ -44,6 +44,7 @@ SIGNATURES = {
     "gdr_chunk_out_noalloc": (ctypes.c_int, [_T, _T, _T, _T, _T, _f32, _vp, _i32, _T, _vp]),
     "gdr_debug_check_cu_seqlens": (ctypes.c_int, [_vp, _i32, _i64, _vp, _vp, _vp]),
     "gdr_device_status": (ctypes.c_int, [_vp]),
+    "gdr_debug_wait_selftest": (ctypes.c_int, [ctypes.c_uint32, _vp]),
     "gdr_clear_device_status": (ctypes.c_int, []),
     "gdr_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gdr_version": (ctypes.c_int, []),

@@ -249,5 +249,10 @@ def device_status() -> int:
     return s.value
 
 
+def wait_selftest(limit_us: int = 2000, stream=None) -> None:
+    """Run the bounded-wait self-test kernel (see gdr_debug_wait_selftest)."""
+    nat.check(nat.lib().gdr_debug_wait_selftest(limit_us, _stream(stream)), "gdr_debug_wait_selftest")
+
+
 def clear_device_status() -> None:
     nat.check(nat.lib().gdr_clear_device_status(), "gdr_clear_device_status")

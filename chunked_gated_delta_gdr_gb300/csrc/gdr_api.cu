@@ -504,6 +504,15 @@ int gdr_device_status(int32_t *status_out) {
   return read_device_status(status_out) == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 
+int gdr_debug_wait_selftest(uint32_t limit_us, cudaStream_t stream) {
+  if (limit_us == 0 || limit_us > 1000000u) return GDR_ERR_SHAPE;
+  int r;
+  if ((r = device_ok())) return r;
+  return launch_wait_selftest(limit_us, GDR_STATUS_WAIT_SELFTEST, stream) == cudaSuccess
+             ? GDR_OK
+             : GDR_ERR_CUDA;
+}
+
 int gdr_clear_device_status(void) {
   return clear_device_status() == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }

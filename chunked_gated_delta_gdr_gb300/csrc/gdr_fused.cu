@@ -1056,6 +1056,28 @@ cudaError_t launch_fused(const FusedArgs &a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+namespace {
+// A bounded wait on an mbarrier that nothing ever arrives on: it must run out
+// after `limit_ns`, record `code` in the status word and return.
+__global__ void k_wait_selftest(uint64_t limit_ns, int32_t code) {
+  __shared__ uint64_t bar;
+  __shared__ int32_t abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const bool done = mbar_wait(&bar, 0, &abort_flag, limit_ns);
+  if (!done && threadIdx.x == 0) atomicCAS(&g_device_status, 0, code);
+}
+}  // namespace
+
+cudaError_t launch_wait_selftest(uint32_t limit_us, int32_t code, cudaStream_t stream) {
+  k_wait_selftest<<<1, 32, 0, stream>>>((uint64_t)limit_us * 1000ull, code);
+  return cudaGetLastError();
+}
+
 cudaError_t read_device_status(int32_t *out) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return e;

@@ -98,6 +98,7 @@ cudaError_t launch_fused(const FusedArgs &a, cudaStream_t stream);
 
 // Device status word (gdr_fused.cu).
 cudaError_t read_device_status(int32_t *out);
+cudaError_t launch_wait_selftest(uint32_t limit_us, int32_t code, cudaStream_t stream);
 cudaError_t clear_device_status();
 
 }  // namespace gdr

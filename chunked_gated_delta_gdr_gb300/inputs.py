@@ -161,6 +161,9 @@ def _lengths_mixed(gen: torch.Generator, total: int):
 
 WORKLOADS = ("tiny", "fixed_b4_t4096_h16", "packed_64k_h32", "long_t20468_h32",
              "gqa_packed_128k_h16x32")
+# A smaller case of the bench workload's shapes, for profiler captures that must
+# stay small (8 segments of 2048 tokens, H = Hk = 32, d = 128, no states).
+PROFILE_WORKLOADS = ("packed_16k_h32",)
 
 
 def make_named(name: str) -> Workload:
@@ -182,6 +185,10 @@ def make_named(name: str) -> Workload:
         gen = torch.Generator().manual_seed(1234 + 4)
         lens = _lengths_mixed(gen, 131072)
         return make_workload(name, 0, lens, 16, 32, 128, with_h0=True, want_ht=True, gen=gen)
+    if name == "packed_16k_h32":
+        gen = torch.Generator().manual_seed(1234 + 100)
+        return make_workload(name, 0, [2048] * 8, 32, 32, 128, with_h0=False, want_ht=False,
+                             gen=gen)
     raise KeyError(name)
 
 

@@ -189,12 +189,25 @@ int gdr_debug_check_cu_seqlens(const int32_t *cu_seqlens, int32_t n_seq, int64_t
 
 /*
  * Device status word of the fused kernel.  Every bounded wait inside the fused
- * kernel that runs out sets a nonzero code here (it then releases what it holds and
- * returns instead of hanging).  gdr_device_status synchronises the current device and
+ * kernel that runs out (after 2 s) sets a nonzero code here: 0x1xx producer,
+ * 0x2xx MMA issuer, 0x3xx prep warps, 0x4xx state warps; the CTA then drains its
+ * copies and MMAs in flight, releases its Tensor Memory and returns instead of
+ * hanging.  gdr_device_status synchronises the current device and
  * reads the word; gdr_clear_device_status resets it.  0 means no wait ran out.
  */
 int gdr_device_status(int32_t *status_out);
 int gdr_clear_device_status(void);
+
+/*
+ * Self-test of the bounded waits: launches one block that waits on an mbarrier
+ * nothing ever arrives on.  The wait gives up after `limit_us` microseconds
+ * (1..1000000), records GDR_STATUS_WAIT_SELFTEST in the device status word (if it
+ * was 0) and the kernel returns normally; the context stays usable.  Read the word
+ * with gdr_device_status.  Errors: GDR_ERR_SHAPE for a limit out of range,
+ * GDR_ERR_DEVICE, GDR_ERR_CUDA.
+ */
+#define GDR_STATUS_WAIT_SELFTEST 0x7001
+int gdr_debug_wait_selftest(uint32_t limit_us, cudaStream_t stream);
 
 /*
  * gdr_chunk_out_noalloc -- gdr_chunk_out for callers that cannot allocate device memory.

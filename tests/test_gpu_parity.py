@@ -261,3 +261,4 @@ def test_named_workload_full_size(name, path):
     assert_o_close(o[:, heads], o_ref, mask)
     if w.want_ht:
         assert_ht_close(ht[:, heads], ht_ref)
+    assert api.device_status() == 0, "a bounded wait ran out"
