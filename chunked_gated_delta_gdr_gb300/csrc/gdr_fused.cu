@@ -2,28 +2,32 @@
 // sm_103a (GB300), plus the device status word.
 //
 // One CTA per SM walks a work list of (segment, value head) units, longest
-// segments first.  For each 64-token chunk of a unit it runs the three stages
-// of the chunkwise (WY) form with every intermediate on chip:
+// segments first.  For each 64-token chunk of a unit it runs the chunkwise (WY)
+// form with every intermediate on chip:
 //
 //   prep   G = cumsum(g); X1 = [K;Q] K^T (KK^T and QK^T);  A, P masks;
-//          Tm = (I + A)^-1;  U^T = V^T (Tm diag(beta))^T;  W^T = K^T (Tm diag(beta e^G))^T
-//   scan   V'^T = U^T - S^T W^T;  S^T <- e^{G_last} S^T + V''^T K,  V'' = diag(e^{G_last-G}) V'
-//   out    O^T = S^T (diag(e^G) Q)^T + V'^T P^T,  P_ij = e^{G_i-G_j} q_i.k_j (j <= i)
+//          Tm = (I + A)^-1;  Tm diag(beta) as a bf16 operand
+//   scan   Y = S^T K^T;  U^T = V^T (Tm diag(beta))^T;  V'^T = U^T - (Y diag(e^G)) (Tm diag(beta))^T
+//          (so V' = U - W S with W = Tm diag(beta e^G) K, never formed);
+//          S^T <- e^{G_last} S^T + V''^T K,  V'' = diag(e^{G_last-G}) V'
+//   out    O^T = e^G-scaled S^T Q^T + V'^T P^T,  P_ij = e^{G_i-G_j} q_i.k_j (j <= i)
 //
 // The state is kept transposed (S^T: value dim on TMEM lanes, key dim on
 // columns) so that every tcgen05.mma has M = 128: the head dimension is the M
-// side and the chunk's 64 tokens are N or K.  Operands are bf16 in 128-byte
-// swizzled shared memory, accumulators fp32 in TMEM.  The chunk size (64) is
-// the one FlashQLA's varlen path uses ("Findings from integrating FlashQLA's
-// Blackwell GDN kernels into a JAX trainer", section 1); a unit with no chunks
-// (a length-0 segment, section 2 of the same page) is never scheduled, so it
-// can store no output.
+// side and the chunk's 64 tokens are N or K.  Operands that come from the state
+// side (S^T, Y, V'^T, V''^T) stay in TMEM as bf16 A operands; the rest are bf16
+// in 128-byte swizzled shared memory; accumulators are fp32 in TMEM.  The chunk
+// size (64) is the one FlashQLA's varlen path uses ("Findings from integrating
+// FlashQLA's Blackwell GDN kernels into a JAX trainer", section 1); a unit with no
+// chunks (a length-0 segment, section 2 of the same page) is never scheduled, so
+// it can store no output.
 //
-// Warp roles (320 threads):
-//   warp 0      TMA producer: K, Q, V tiles and g, beta of each chunk into a 2-stage ring
-//   warp 1      MMA issuer (one thread) and TMEM owner
-//   warps 2-5   prep warpgroup (one TMEM lane quadrant per warp)
-//   warps 6-9   state warpgroup
+// Warp roles (352 threads):
+//   warp 0      TMA producer: K, Q, V tiles and g, beta of each chunk into a 3-stage ring
+//   warp 1      MMA issuer P (one thread: X1, U, O1, O2) and TMEM owner
+//   warp 2      MMA issuer C (one thread: Y, V', S update)
+//   warps 3-6   prep warpgroup (one TMEM lane quadrant per warp)
+//   warps 7-10  state warpgroup: bf16 conversions on the state chain, output epilogue
 // Every wait is bounded in time; a wait that runs out sets the device status
 // word and a CTA-wide abort flag, each role drains what it has in flight and
 // the CTA releases its TMEM and exits.
@@ -42,8 +46,8 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 320;
-constexpr int kStages = 2;
+constexpr int kThreads = 352;
+constexpr int kStages = 3;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kUnitRing = 4;
 
@@ -52,24 +56,23 @@ constexpr uint32_t kKQBytes = 32768;  // 2 key blocks x [K rows 0-63 | Q rows 64
 constexpr uint32_t kVBytes = 16384;   // 2 value blocks x 64 rows x 128 B
 constexpr uint32_t kStageBytes = kKQBytes + kVBytes;
 constexpr uint32_t OFF_STAGE = 0;
-constexpr uint32_t OFF_ST = OFF_STAGE + kStages * kStageBytes;  // S^T bf16, 2 key blocks x 128 rows
-constexpr uint32_t OFF_WT = OFF_ST + 32768;                     // W^T bf16, 128 rows (dk) x 64 tok
-constexpr uint32_t OFF_P = OFF_WT + 16384;                      // P bf16, 2 buffers of 64 x 64
-constexpr uint32_t OFF_VT = OFF_P + 16384;                      // V'^T bf16, 128 rows (dv) x 64 tok
-constexpr uint32_t OFF_VS = OFF_VT + 16384;                     // V''^T bf16; output staging
-constexpr uint32_t OFF_A = OFF_VS + 16384;                      // solve scratch fp32 64 x 65
-constexpr uint32_t OFF_TB = OFF_A;           // Tm diag(beta) bf16 64 x 64, aliases the scratch
-constexpr uint32_t OFF_TBG = OFF_A + 8192;   // Tm diag(beta e^G) bf16, aliases the scratch
-constexpr uint32_t OFF_Y = OFF_A + 17408;    // solve scratch fp32 32 x 40
+constexpr uint32_t OFF_P = OFF_STAGE + kStages * kStageBytes;  // P bf16, 2 buffers of 64 x 64
+constexpr uint32_t OFF_TB = OFF_P + 16384;     // Tm diag(beta) bf16 64 x 64
+constexpr uint32_t OFF_STG = OFF_TB + 8192;    // output staging [64 tokens][128 dv] bf16
+constexpr uint32_t OFF_A = OFF_STG + 16384;    // solve scratch fp32 64 x kLdA
+constexpr uint32_t OFF_Y = OFF_A + 17408;      // solve scratch fp32 32 x kLdY
 constexpr uint32_t OFF_SMALL = OFF_Y + 5120;
-constexpr uint32_t kSmemBytes = OFF_SMALL + 4096 + 1024;  // + small arrays + alignment slack
+constexpr uint32_t kSmallBytes = 9216;
+constexpr uint32_t kSmemBytes = OFF_SMALL + kSmallBytes + 1024;  // + alignment slack
 constexpr int kLdA = 68, kLdY = 40, kLdX = 24;  // padded leading dims of the fp32 scratch
+static_assert(kSmemBytes <= 232448, "shared memory over the per-block limit");
 
 // ---- TMEM columns ----
 constexpr uint32_t TM_S = 0;     // S^T fp32, 128 columns (key dim)
-constexpr uint32_t TM_X1 = 128;  // [KK^T ; QK^T], 64 columns
-constexpr uint32_t TM_U0 = 192;  // U^T / V'^T, two buffers of 64 columns
-constexpr uint32_t TM_W = 320;   // W^T, 64 columns
+constexpr uint32_t TM_SB = 128;  // S^T bf16 pairs (A operand), 64 columns
+constexpr uint32_t TM_U = 192;   // two buffers of 64 columns, by chunk parity: X1, then U^T ->
+                                 // V'^T fp32, then bf16 V'^T (cols 0-31) and V''^T (32-63)
+constexpr uint32_t TM_Y = 320;   // Y = S^T K^T fp32, then -Y diag(e^G) as bf16 pairs in cols 0-31
 constexpr uint32_t TM_O = 384;   // S^T Q^T (inter-chunk part of O^T), 64 columns
 constexpr uint32_t TM_O2 = 448;  // V'^T P^T (intra-chunk part of O^T), 64 columns
 constexpr uint32_t kTmemCols = 512;
@@ -78,29 +81,37 @@ struct UnitInfo {
   int32_t seq, head, t0, end, nch, pad0, pad1, pad2;
 };
 
-// Per-chunk vectors, computed by the producer warp from g and beta.  Three
-// slots (by chunk index) keep a chunk's vectors alive until its output epilogue.
-constexpr int kInfo = 3;
+// Per-chunk vectors, computed by the producer warp from g and beta.  Five slots
+// (by chunk index): the producer refills chunk c's slot for chunk c+5 only after
+// chunk c+2's stage is released, which follows chunk c's output epilogue.
+constexpr int kInfo = 5;
 struct ChunkVec {
   alignas(16) float G[64];     // chunk-local inclusive cumsum of g, times log2(e)
   alignas(16) float eG[64];    // exp(G_j)
+  alignas(16) float eGs[64];   // scale * exp(G_j)
+  alignas(16) float bfac[64];  // 2^(Gref - G_j) (valid when fac != 0)
   alignas(16) float dec[64];   // exp(G_last - G_j)
   alignas(16) float beta[64];  // beta (0 past the chunk's end)
   float eL;                    // exp(G_last)
-  float pad[3];
+  float Gref;                  // max_j G_j
+  int32_t fac;                 // 1: max G - min G is small enough to factor 2^(G_i - G_j)
+  float pad;
 };
+// 2^(G_i - G_j) = 2^(G_i - Gref) 2^(Gref - G_j) with both factors normal fp32 numbers
+// as long as the chunk's range of G (log2 units) stays below this bound.
+constexpr float kFacRange = 100.f;
 
 struct Small {
   uint64_t full[kStages], empty[kStages];
-  uint64_t x1_full, x1_free, t_ready, uw_full, wt_ready, s_ready, vp_full, vp_ready, s_full,
-      o_full, o_free, drain;
+  uint64_t x1_full, x1_free, t_ready, uw_full, s_ready, y_full, y_ready, vp_full, vp_ready,
+      s_full, o1_full, o_full, o_free, drain;
   uint64_t unit_full[kUnitRing], unit_empty[kUnitRing];
   UnitInfo unit[kUnitRing];
   ChunkVec cv[kInfo];
   uint32_t tmem_base;
   int32_t abort;
 };
-static_assert(sizeof(Small) <= 4096, "small area too large");
+static_assert(sizeof(Small) <= kSmallBytes, "small area too large");
 
 struct Params {
   int32_t T, n_seq, Hk, H, D, has_h0;
@@ -121,7 +132,7 @@ struct Params {
 };
 
 // ------------------------------------------------------------------ helpers
-__device__ __forceinline__ void fail(Small *sm, int code) {
+__device__ __noinline__ void fail(Small *sm, int code) {
   sm->abort = 1;
   atomicCAS(&g_device_status, 0, code);
 }
@@ -263,8 +274,8 @@ __device__ void role_producer(const Params &p, Small *sm, uint8_t *base,
         }
       }
       {
-        // chunk-local cumsum of g and the decay vectors; the slot (chunk g mod 3) was
-        // last read by chunk g-3's output epilogue, which precedes the stage release
+        // chunk-local cumsum of g and the decay vectors (the slot's previous chunk is
+        // done: see kInfo)
         ChunkVec &cv = sm->cv[g % kInfo];
         float sum = g0 + g1;
 #pragma unroll
@@ -276,15 +287,31 @@ __device__ void role_producer(const Params &p, Small *sm, uint8_t *base,
         constexpr float kLog2e = 1.4426950408889634f;
         const float G0 = (sum - g1) * kLog2e, G1 = sum * kLog2e;
         const float GL = __shfl_sync(0xffffffffu, G1, 31);
+        float gmax = fmaxf(G0, G1), gmin = fminf(G0, G1);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+          gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, off));
+          gmin = fminf(gmin, __shfl_xor_sync(0xffffffffu, gmin, off));
+        }
+        const bool fac = gmax - gmin <= kFacRange;
         cv.G[j0] = G0;
         cv.G[j1] = G1;
-        cv.eG[j0] = ex2(G0);
-        cv.eG[j1] = ex2(G1);
+        const float e0 = ex2(G0), e1 = ex2(G1);
+        cv.eG[j0] = e0;
+        cv.eG[j1] = e1;
+        cv.eGs[j0] = p.scale * e0;
+        cv.eGs[j1] = p.scale * e1;
+        cv.bfac[j0] = fac ? ex2(gmax - G0) : 0.f;
+        cv.bfac[j1] = fac ? ex2(gmax - G1) : 0.f;
         cv.dec[j0] = ex2(GL - G0);
         cv.dec[j1] = ex2(GL - G1);
         cv.beta[j0] = b0;
         cv.beta[j1] = b1;
-        if (lane == 0) cv.eL = ex2(GL);
+        if (lane == 0) {
+          cv.eL = ex2(GL);
+          cv.Gref = gmax;
+          cv.fac = fac ? 1 : 0;
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm->full[s]);
@@ -297,23 +324,42 @@ __device__ void role_producer(const Params &p, Small *sm, uint8_t *base,
   }
 }
 
-__device__ void role_mma(const Params &p, Small *sm, uint8_t *base) {
+// MMA issue is split over two threads in different warps, because one thread
+// issues a tcgen05.mma only every ~100 cycles whatever its size.  Issuer P
+// runs the MMAs off the state chain (X1, U, O1, O2); issuer C runs the chain
+// (Y, V', S update).  A stage is released once both have committed.
+__device__ void issuer_drain(Small *sm) {
+  mma_commit(&sm->drain);
+  mbar_wait(&sm->drain, 0, nullptr, kWaitLimitNs);
+}
+
+__device__ void role_issue_p(const Params &p, Small *sm, uint8_t *base) {
   const uint32_t tb = sm->tmem_base;
   const uint32_t sbase = smem_u32(base);
   const uint32_t id_x1 = idesc_bf16(128, 64, false, false);
-  const uint32_t id_uw = idesc_bf16(128, 64, true, false);
-  const uint32_t id_vp = idesc_bf16(128, 64, false, true, true);
-  const uint32_t id_o1 = idesc_bf16(128, 64, false, false);
-  const uint32_t id_su = idesc_bf16(128, 128, false, true);
-  const uint32_t id_o2 = idesc_bf16(128, 64, false, false);
+  const uint32_t id_uw = idesc_bf16(128, 64, true, false);  // A = V^T (MN-major)
+  const uint32_t id_n64 = idesc_bf16(128, 64, false, false);
   uint32_t g = 0;
   bool ok = true;
+  // X1 of chunk gg into its U buffer (by parity).  It needs its stage, prep done
+  // reading X1 of chunk gg-1 (one x1_full phase at a time), and chunk gg-2's
+  // MMAs (the last readers of that U buffer and of the P buffer) complete, i.e.
+  // chunk gg-2's stage released.
+  auto x1_wait = [&](uint32_t gg, int code) {
+    if (!wait1(sm, sm->full[gg % kStages], (gg / kStages) & 1, code)) return false;
+    if (gg >= 1 && !wait1(sm, sm->x1_free, (gg - 1) & 1, code + 1)) return false;
+    if (gg >= 2 && !wait1(sm, sm->empty[(gg - 2) % kStages], ((gg - 2) / kStages) & 1, code + 2))
+      return false;
+    tc_fence_after();
+    return true;
+  };
   auto issue_x1 = [&](uint32_t gg) {
     const uint32_t kq = sbase + OFF_STAGE + (gg % kStages) * kStageBytes;
-#pragma unroll
+    const uint32_t d = tb + TM_U + (gg & 1) * 64;
+#pragma unroll 1
     for (int kk = 0; kk < 8; ++kk) {
       const uint32_t a = kq + (kk / 4) * 16384 + (kk % 4) * 32;
-      mma_bf16(tb + TM_X1, sdesc_sw128(a, 0, 1024), sdesc_sw128(a, 0, 1024), id_x1, kk > 0);
+      mma_bf16(d, sdesc_sw128(a, 0, 1024), sdesc_sw128(a, 0, 1024), id_x1, kk > 0);
     }
     mma_commit(&sm->x1_full);
   };
@@ -327,91 +373,97 @@ __device__ void role_mma(const Params &p, Small *sm, uint8_t *base) {
       const uint32_t s = g % kStages;
       const uint32_t kq = sbase + OFF_STAGE + s * kStageBytes;
       const uint32_t vv = kq + kKQBytes;
+      const uint32_t tu = tb + TM_U + (g & 1) * 64;
       if (c == 0) {
-        if (!wait1(sm, sm->full[s], (g / kStages) & 1, 0x202)) { ok = false; break; }
-        if (g >= 1 && !wait1(sm, sm->x1_free, (g - 1) & 1, 0x203)) { ok = false; break; }
-        tc_fence_after();
+        if (!x1_wait(g, 0x202)) { ok = false; break; }
         issue_x1(g);
       }
-      // U^T = V^T (Tm diag beta)^T ; W^T = K^T (Tm diag(beta e^G))^T
-      if (!wait1(sm, sm->t_ready, g & 1, 0x204)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t tu = tb + TM_U0 + (g & 1) * 64;
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        mma_bf16(tu, sdesc_sw128(vv + kk * 2048, 8192, 1024),
-                 sdesc_sw128(sbase + OFF_TB + kk * 32, 0, 1024), id_uw, kk > 0);
-      }
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        mma_bf16(tb + TM_W, sdesc_sw128(kq + kk * 2048, 16384, 1024),
-                 sdesc_sw128(sbase + OFF_TBG + kk * 32, 0, 1024), id_uw, kk > 0);
-      }
-      mma_commit(&sm->uw_full);
-      // next chunk's X1 (prep of c+1 overlaps this chunk's scan): issued as soon as
-      // its stage has landed, without holding up this chunk's scan MMAs
-      bool x1_pending = c + 1 < ui.nch;
-      const uint32_t s1 = (g + 1) % kStages, ph1 = ((g + 1) / kStages) & 1;
-      auto try_x1 = [&]() {
-        if (x1_pending && mbar_test(&sm->full[s1], ph1) && mbar_test(&sm->x1_free, g & 1)) {
-          tc_fence_after();
-          issue_x1(g + 1);
-          x1_pending = false;
-        }
-      };
-      try_x1();
-      // V'^T = U^T - S^T W^T
-      if (!wait1(sm, sm->s_ready, g & 1, 0x207)) { ok = false; break; }
-      if (!wait1(sm, sm->wt_ready, g & 1, 0x208)) { ok = false; break; }
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        mma_bf16(tu, sdesc_sw128(sbase + OFF_ST + (kk / 4) * 16384 + (kk % 4) * 32, 0, 1024),
-                 sdesc_sw128(sbase + OFF_WT + kk * 2048, 16384, 1024), id_vp, 1);
-      }
-      mma_commit(&sm->vp_full);
-      try_x1();
-      // O^T = S^T Q~^T
-      if (g >= 1 && !wait1(sm, sm->o_free, (g - 1) & 1, 0x209)) { ok = false; break; }
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        mma_bf16(tb + TM_O,
-                 sdesc_sw128(sbase + OFF_ST + (kk / 4) * 16384 + (kk % 4) * 32, 0, 1024),
-                 sdesc_sw128(kq + (kk / 4) * 16384 + 8192 + (kk % 4) * 32, 0, 1024), id_o1,
-                 kk > 0);
-      }
-      try_x1();
-      // S^T += V''^T K ;  O^T += V'^T P^T
-      if (!wait1(sm, sm->vp_ready, g & 1, 0x20a)) { ok = false; break; }
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        mma_bf16(tb + TM_S, sdesc_sw128(sbase + OFF_VS + kk * 32, 0, 1024),
-                 sdesc_sw128(kq + kk * 2048, 16384, 1024), id_su, 1);
-      }
-      mma_commit(&sm->s_full);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        mma_bf16(tb + TM_O2, sdesc_sw128(sbase + OFF_VT + kk * 32, 0, 1024),
-                 sdesc_sw128(sbase + OFF_P + (g & 1) * 8192 + kk * 32, 0, 1024), id_o2, kk > 0);
-      }
-      mma_commit(&sm->o_full);
-      mma_commit(&sm->empty[s]);
-      if (x1_pending) {
-        if (!wait1(sm, sm->full[s1], ph1, 0x205)) { ok = false; break; }
-        if (!wait1(sm, sm->x1_free, g & 1, 0x206)) { ok = false; break; }
-        tc_fence_after();
+      // next chunk's X1 first: prep of c+1 starts as soon as prep of c ends
+      if (c + 1 < ui.nch) {
+        if (!x1_wait(g + 1, 0x205)) { ok = false; break; }
         issue_x1(g + 1);
       }
+      // U^T = V^T (Tm diag beta)^T
+      if (!wait1(sm, sm->t_ready, g & 1, 0x208)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll 1
+      for (int kk = 0; kk < 4; ++kk)
+        mma_bf16(tu, sdesc_sw128(vv + kk * 2048, 8192, 1024),
+                 sdesc_sw128(sbase + OFF_TB + kk * 32, 0, 1024), id_uw, kk > 0);
+      mma_commit(&sm->uw_full);
+      // O^T (inter-chunk part) = S^T Q^T, once the epilogue has read the previous chunk's
+      if (!wait1(sm, sm->s_ready, g & 1, 0x209)) { ok = false; break; }
+      if (g >= 1 && !wait1(sm, sm->o_free, (g - 1) & 1, 0x20a)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll 1
+      for (int kk = 0; kk < 8; ++kk)
+        mma_bf16_ts(tb + TM_O, tb + TM_SB + kk * 8,
+                    sdesc_sw128(kq + (kk / 4) * 16384 + 8192 + (kk % 4) * 32, 0, 1024), id_n64,
+                    kk > 0);
+      mma_commit(&sm->o1_full);  // the bf16 copy of S^T is free as far as O1 goes
+      // O2^T = V'^T P^T
+      if (!wait1(sm, sm->vp_ready, g & 1, 0x20b)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll 1
+      for (int kk = 0; kk < 4; ++kk)
+        mma_bf16_ts(tb + TM_O2, tu + kk * 8,
+                    sdesc_sw128(sbase + OFF_P + (g & 1) * 8192 + kk * 32, 0, 1024), id_n64,
+                    kk > 0);
+      mma_commit(&sm->o_full);
+      mma_commit(&sm->empty[s]);
     }
   }
-  // drain: every MMA issued so far must finish before TMEM is released
-  mma_commit(&sm->drain);
-  mbar_wait(&sm->drain, 0, nullptr, kWaitLimitNs);
+  issuer_drain(sm);
 }
 
-// Pack eight fp32 values as bf16 into one 16-byte chunk of a swizzled tile row.
+__device__ void role_issue_c(const Params &p, Small *sm, uint8_t *base) {
+  const uint32_t tb = sm->tmem_base;
+  const uint32_t sbase = smem_u32(base);
+  const uint32_t id_n64 = idesc_bf16(128, 64, false, false);
+  const uint32_t id_su = idesc_bf16(128, 128, false, true);  // B = K (MN-major)
+  uint32_t g = 0;
+  bool ok = true;
+  for (uint32_t k = 0; ok; ++k) {
+    const int slot = k % kUnitRing;
+    if (!wait1(sm, sm->unit_full[slot], (k / kUnitRing) & 1, 0x211)) { ok = false; break; }
+    const UnitInfo ui = sm->unit[slot];
+    mbar_arrive(&sm->unit_empty[slot]);
+    if (ui.seq < 0) break;
+    for (int c = 0; c < ui.nch; ++c, ++g) {
+      const uint32_t s = g % kStages;
+      const uint32_t kq = sbase + OFF_STAGE + s * kStageBytes;
+      const uint32_t tu = tb + TM_U + (g & 1) * 64;
+      // Y = S^T K^T  (S before this chunk, bf16 in TMEM)
+      if (!wait1(sm, sm->s_ready, g & 1, 0x212)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll 1
+      for (int kk = 0; kk < 8; ++kk)
+        mma_bf16_ts(tb + TM_Y, tb + TM_SB + kk * 8,
+                    sdesc_sw128(kq + (kk / 4) * 16384 + (kk % 4) * 32, 0, 1024), id_n64, kk > 0);
+      mma_commit(&sm->y_full);
+      // V'^T = U^T + (-Y diag(e^G)) (Tm diag(beta))^T
+      if (!wait1(sm, sm->y_ready, g & 1, 0x213)) { ok = false; break; }
+      if (!wait1(sm, sm->uw_full, g & 1, 0x214)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll 1
+      for (int kk = 0; kk < 4; ++kk)
+        mma_bf16_ts(tu, tb + TM_Y + kk * 8, sdesc_sw128(sbase + OFF_TB + kk * 32, 0, 1024),
+                    id_n64, 1);
+      mma_commit(&sm->vp_full);
+      // S^T += V''^T K
+      if (!wait1(sm, sm->vp_ready, g & 1, 0x215)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll 1
+      for (int kk = 0; kk < 4; ++kk)
+        mma_bf16_ts(tb + TM_S, tu + 32 + kk * 8, sdesc_sw128(kq + kk * 2048, 16384, 1024), id_su,
+                    1);
+      mma_commit(&sm->s_full);
+      mma_commit(&sm->empty[s]);
+    }
+  }
+  issuer_drain(sm);
+}
+
 __device__ __forceinline__ void store_chunk8(uint32_t tile, int row, int col, const float *v) {
   st_shared_v4(tile + sw128_off(row, col), pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]),
                pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
@@ -506,35 +558,42 @@ __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
       if (!wait_wg(sm, sm->x1_full, g & 1, 0x303, kBarPrep)) { ok = false; break; }
       tc_fence_after();
       {
+        // A_ij = beta_i e^{G_i-G_j} k_i.k_j (j < i);  P_ij = scale e^{G_i-G_j} q_i.k_j (j <= i)
         const int i = row & 63;
-        const float *Gc = cv.G;
-        const float gi = Gc[i];
         const bool live = i < len;
-        const float scl = (row < 64) ? cv.beta[i] : 1.f;
+        const bool is_a = row < 64;
+        const float scl = is_a ? cv.beta[i] : p.scale;
+        const int lim = is_a ? i : i + 1;
+        const bool fac = cv.fac != 0;  // same for the whole chunk
+        const float gi = cv.G[i];
+        const float ci = fac ? scl * ex2(gi - cv.Gref) : scl;
+        const uint32_t tx1 = tb + TM_U + (g & 1) * 64;
 #pragma unroll 1
-        for (int h = 0; h < 4; ++h) {  // 16 columns at a time
-          uint32_t r[16];
-          tmem_ld16(tmem_addr(tb + TM_X1, lane_base, h * 16), r);
-          float gv[16];
+        for (int hh = 0; hh < 2; ++hh) {  // 32 columns at a time
+          uint32_t r[32];
+          tmem_ld32(tmem_addr(tx1, lane_base, hh * 32), r);
+          float f[32];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) ld_f4(Gc + h * 16 + q * 4, gv + q * 4);
+          for (int q = 0; q < 8; ++q) ld_f4((fac ? cv.bfac : cv.G) + hh * 32 + q * 4, f + q * 4);
+          if (!fac) {
+#pragma unroll
+            for (int u = 0; u < 32; ++u) f[u] = ex2(gi - f[u]);
+          }
           tmem_ld_wait();
-          const int lim = (row < 64) ? i : i + 1;  // A: j < i, P: j <= i
-          float v[16];
+          float v[32];
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const int j = h * 16 + u;
-            const float e = ex2(gi - gv[u]);
-            const float prod = scl * e * __uint_as_float(r[u]);
+          for (int u = 0; u < 32; ++u) {
+            const int j = hh * 32 + u;
+            const float prod = (ci * f[u]) * __uint_as_float(r[u]);
             v[u] = (live && j < lim) ? prod : 0.f;
           }
-          if (row < 64) {
+          if (is_a) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) st_f4(AS + i * kLdA + h * 16 + q * 4, v + q * 4);
+            for (int q = 0; q < 8; ++q) st_f4(AS + i * kLdA + hh * 32 + q * 4, v + q * 4);
           } else {
             const uint32_t ptile = sbase + OFF_P + cb2 * 8192;
-            store_chunk8(ptile, i, h * 16, v);
-            store_chunk8(ptile, i, h * 16 + 8, v + 8);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) store_chunk8(ptile, i, hh * 32 + q * 8, v + q * 8);
           }
         }
       }
@@ -599,8 +658,8 @@ __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
         warp_store16(AS + (32 + 16 * mt) * kLdA + 16 * nt, kLdA, acc2, -1.f);
       }
       named_bar(kBarPrep, 128);
-      // Tm diag(beta) and Tm diag(beta e^G) as bf16 operands, half a row per thread;
-      // they overwrite the scratch, so every row is read before any is written
+      // Tm diag(beta) as a bf16 operand, half a row per thread, once the previous
+      // chunk's MMAs that read it are done
       {
         const int ri = pid & 63, hc = (pid >> 6) * 32;
         float v[32];
@@ -612,63 +671,65 @@ __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
 #pragma unroll
           for (int u = 0; u < 4; ++u) v[q * 4 + u] = (hc + q * 4 + u <= ri) ? tq[u] * bq[u] : 0.f;
         }
-        named_bar(kBarPrep, 128);
+        if (g >= 1 && !wait_wg(sm, sm->vp_full, (g - 1) & 1, 0x305, kBarPrep)) { ok = false; break; }
 #pragma unroll
         for (int q = 0; q < 4; ++q) store_chunk8(sbase + OFF_TB, ri, hc + q * 8, v + q * 8);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          float eq[4];
-          ld_f4(cv.eG + hc + q * 4, eq);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) v[q * 4 + u] *= eq[u];
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) store_chunk8(sbase + OFF_TBG, ri, hc + q * 8, v + q * 8);
       }
       fence_async_smem();
       mbar_arrive(&sm->t_ready);
-      // W^T (lane = key dim) -> bf16 operand; waits until the previous V'^T MMA read it
-      if (!wait_wg(sm, sm->uw_full, g & 1, 0x305, kBarPrep)) { ok = false; break; }
-      if (g >= 1 && !wait_wg(sm, sm->vp_full, (g - 1) & 1, 0x306, kBarPrep)) { ok = false; break; }
-      tc_fence_after();
-      {
-        uint32_t r0[32], r1[32];
-        tmem_ld32(tmem_addr(tb + TM_W, lane_base, 0), r0);
-        tmem_ld32(tmem_addr(tb + TM_W, lane_base, 32), r1);
-        tmem_ld_wait();
-        float v[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u) v[u] = __uint_as_float(q < 4 ? r0[q * 8 + u] : r1[(q - 4) * 8 + u]);
-          store_chunk8(sbase + OFF_WT, row, q * 8, v);
-        }
-      }
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(&sm->wt_ready);
     }
   }
 }
 
+// Pack 64 fp32 values (two TMEM loads of 32 columns) into 32 bf16 pairs.
+__device__ __forceinline__ void pack64(const uint32_t (&a)[32], const uint32_t (&b)[32],
+                                       uint32_t (&o)[32]) {
+#pragma unroll
+  for (int u = 0; u < 16; ++u) {
+    o[u] = pack_bf16(__uint_as_float(a[2 * u]), __uint_as_float(a[2 * u + 1]));
+    o[16 + u] = pack_bf16(__uint_as_float(b[2 * u]), __uint_as_float(b[2 * u + 1]));
+  }
+}
+
+// Row dv of the unit's initial state (S^T row = column dv of h0, zero without h0)
+// into TMEM; once per unit, so kept out of line.
+__device__ __noinline__ void state_from_h0(const Params &p, uint32_t taddr, int64_t sidx, int dv) {
+  const int D = p.D;
+  const bool from_h0 = p.has_h0 && dv < D;
+#pragma unroll 1
+  for (int cb = 0; cb < 4; ++cb) {
+    uint32_t r[32];
+#pragma unroll
+    for (int u = 0; u < 32; ++u) {
+      const int j = cb * 32 + u;
+      r[u] = __float_as_uint((from_h0 && j < D) ? p.h0[sidx + (int64_t)j * D + dv] : 0.f);
+    }
+    tmem_st32(taddr + cb * 32, r);
+  }
+  tmem_st_wait();
+}
+
 // The state warpgroup.  `row` is this thread's TMEM lane = value dimension dv.
+// Per chunk: S^T -> bf16 (A operand of Y and O1) and e^{G_last} S^T; Y -> bf16;
+// V'^T -> bf16 V'^T and V''^T; and the previous chunk's output.
 __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
   const uint32_t tb = sm->tmem_base;
-  const uint32_t sbase = smem_u32(base);
   const uint32_t lane_base = (uint32_t)(row & ~31);
   const int dv = row;
   const int D = p.D;
-  uint8_t *stage_o = base + OFF_VS;  // output staging [64 tokens][128 dv] bf16
+  uint8_t *stage_o = base + OFF_STG;  // output staging [64 tokens][128 dv] bf16
   uint32_t g = 0;
   bool ok = true;
   int prev_t = 0, prev_len = 0, prev_head = 0;
-  auto epilogue = [&](uint32_t gg) -> bool {
+  // output of chunk gg, part 1: O = scale e^{G_i} (S^T Q^T)_i + (V'^T P^T)_i (P carries
+  // the scale) from TMEM into the staging tile (frees the accumulators early)
+  auto epi_read = [&](uint32_t gg) -> bool {
     if (!wait_wg(sm, sm->o_full, gg & 1, 0x401, kBarState)) return false;
     tc_fence_after();
-    const float *eG = sm->cv[gg % kInfo].eG;
+    const float *eG = sm->cv[gg % kInfo].eGs;
     __nv_bfloat16 *st = reinterpret_cast<__nv_bfloat16 *>(stage_o) + dv;
 #pragma unroll 1
-    for (int hb = 0; hb < 2; ++hb) {  // O = scale (e^{G_i} (S^T Q^T)_i + (V'^T P^T)_i)
+    for (int hb = 0; hb < 2; ++hb) {
       uint32_t r1[32], r2[32];
       tmem_ld32(tmem_addr(tb + TM_O, lane_base, hb * 32), r1);
       tmem_ld32(tmem_addr(tb + TM_O2, lane_base, hb * 32), r2);
@@ -682,9 +743,13 @@ __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
       }
 #pragma unroll
       for (int u = 0; u < 32; ++u)
-        st[(hb * 32 + u) * 128] = __float2bfloat16_rn(
-            p.scale * fmaf(e[u], __uint_as_float(r1[u]), __uint_as_float(r2[u])));
+        st[(hb * 32 + u) * 128] =
+            __float2bfloat16_rn(fmaf(e[u], __uint_as_float(r1[u]), __uint_as_float(r2[u])));
     }
+    return true;
+  };
+  // part 2: the staging tile to global memory, 16 bytes per store
+  auto epi_store = [&]() {
     named_bar(kBarState, 128);
     const int chunks_per_row = D / 8;
 #pragma unroll 2
@@ -696,7 +761,6 @@ __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
                                    (int64_t)prev_head * p.o_sh + ch * 8) = val;
       }
     }
-    return true;
   };
   for (uint32_t k = 0; ok; ++k) {
     const int slot = k % kUnitRing;
@@ -705,41 +769,32 @@ __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
     mbar_arrive(&sm->unit_empty[slot]);
     if (ui.seq < 0) break;
     const int64_t sidx = ((int64_t)ui.seq * p.H + ui.head) * D * D;
+    // row dv of S^T, key columns [c0, c0 + 64)
+    auto load_s = [&](int c0, uint32_t (&r0)[32], uint32_t (&r1)[32]) {
+      tmem_ld32(tmem_addr(tb + TM_S, lane_base, c0), r0);
+      tmem_ld32(tmem_addr(tb + TM_S, lane_base, c0 + 32), r1);
+      tmem_ld_wait();
+    };
     for (int c = 0; c < ui.nch; ++c, ++g) {
       const int t = ui.t0 + c * kChunk;
       const int len = min(kChunk, ui.end - t);
-      const int cb2 = g & 1;
-      if (!wait_wg(sm, sm->t_ready, g & 1, 0x403, kBarState)) { ok = false; break; }
-      const float eL = sm->cv[g % kInfo].eL;
-      if (c >= 1) {
-        if (!wait_wg(sm, sm->s_full, (g - 1) & 1, 0x404, kBarState)) { ok = false; break; }
-        tc_fence_after();
-      }
-      // row dv of S^T -> bf16 operand; e^{G_last} S^T back into TMEM
+      // the chunk's vectors are written before its stage is marked full
+      if (!wait_wg(sm, sm->full[g % kStages], (g / kStages) & 1, 0x403, kBarState)) { ok = false; break; }
+      const ChunkVec &cv = sm->cv[g % kInfo];
+      if (c >= 1 && !wait_wg(sm, sm->s_full, (g - 1) & 1, 0x404, kBarState)) { ok = false; break; }
+      // the bf16 copy of S^T is rewritten once the previous chunk's O1 has read it
+      if (g >= 1 && !wait_wg(sm, sm->o1_full, (g - 1) & 1, 0x408, kBarState)) { ok = false; break; }
+      tc_fence_after();
+      if (c == 0) state_from_h0(p, tmem_addr(tb + TM_S, lane_base, 0), sidx, dv);
+      // S^T -> bf16 pairs (A operand of Y and O1), and e^{G_last} S^T (the base of this
+      // chunk's S^T += V''^T K) back in place
+      const float eL = cv.eL;
 #pragma unroll 1
-      for (int hb = 0; hb < 2; ++hb) {  // 64 key columns at a time
-        uint32_t r0[32], r1[32];
-        if (c == 0) {
-#pragma unroll
-          for (int u = 0; u < 32; ++u) {
-            const int j0 = hb * 64 + u, j1 = hb * 64 + 32 + u;
-            const bool in = p.has_h0 && dv < D;
-            r0[u] = __float_as_uint((in && j0 < D) ? p.h0[sidx + (int64_t)j0 * D + dv] : 0.f);
-            r1[u] = __float_as_uint((in && j1 < D) ? p.h0[sidx + (int64_t)j1 * D + dv] : 0.f);
-          }
-        } else {
-          tmem_ld32(tmem_addr(tb + TM_S, lane_base, hb * 64), r0);
-          tmem_ld32(tmem_addr(tb + TM_S, lane_base, hb * 64 + 32), r1);
-          tmem_ld_wait();
-        }
-        const uint32_t tile = sbase + OFF_ST + hb * 16384;
-        float v[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u) v[u] = __uint_as_float(q < 4 ? r0[q * 8 + u] : r1[(q - 4) * 8 + u]);
-          store_chunk8(tile, dv, q * 8, v);
-        }
+      for (int hb = 0; hb < 2; ++hb) {
+        uint32_t r0[32], r1[32], pk[32];
+        load_s(hb * 64, r0, r1);
+        pack64(r0, r1, pk);
+        tmem_st32(tmem_addr(tb + TM_SB, lane_base, hb * 32), pk);
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
           r0[u] = __float_as_uint(__uint_as_float(r0[u]) * eL);
@@ -749,34 +804,62 @@ __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
         tmem_st32(tmem_addr(tb + TM_S, lane_base, hb * 64 + 32), r1);
       }
       tmem_st_wait();
-      fence_async_smem();
       tc_fence_before();
       mbar_arrive(&sm->s_ready);
-      // previous chunk's output (same unit) while this chunk's V'^T is computed
-      if (c >= 1 && !epilogue(g - 1)) { ok = false; break; }
-      if (!wait_wg(sm, sm->vp_full, g & 1, 0x405, kBarState)) { ok = false; break; }
+      // previous chunk's output accumulators (same unit) -> staging, while Y is computed
+      if (c >= 1 && !epi_read(g - 1)) { ok = false; break; }
+      // -Y diag(e^G) -> bf16 pairs in place; token columns past the chunk's end are
+      // zeroed so that whatever the stage holds there cannot reach V'
+      if (!wait_wg(sm, sm->y_full, g & 1, 0x405, kBarState)) { ok = false; break; }
       tc_fence_after();
       {
-        uint32_t r0[32], r1[32];
-        const uint32_t tu = tb + TM_U0 + (g & 1) * 64;
-        tmem_ld32(tmem_addr(tu, lane_base, 0), r0);
-        tmem_ld32(tmem_addr(tu, lane_base, 32), r1);
-        const float *dec = sm->cv[g % kInfo].dec;
-        tmem_ld_wait();
-        float v[8], d[8];
+        uint32_t r0[32], r1[32], pk[32];
+        tmem_ld32(tmem_addr(tb + TM_Y, lane_base, 0), r0);
+        tmem_ld32(tmem_addr(tb + TM_Y, lane_base, 32), r1);
+        float e0[32], e1[32];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u) v[u] = __uint_as_float(q < 4 ? r0[q * 8 + u] : r1[(q - 4) * 8 + u]);
-          store_chunk8(sbase + OFF_VT, dv, q * 8, v);
-          ld_f4(dec + q * 8, d);
-          ld_f4(dec + q * 8 + 4, d + 4);
-#pragma unroll
-          for (int u = 0; u < 8; ++u) v[u] *= d[u];
-          store_chunk8(sbase + OFF_VS, dv, q * 8, v);
+          ld_f4(cv.eG + q * 4, e0 + q * 4);
+          ld_f4(cv.eG + 32 + q * 4, e1 + q * 4);
         }
+        tmem_ld_wait();
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+          r0[u] = __float_as_uint(u < len ? -e0[u] * __uint_as_float(r0[u]) : 0.f);
+          r1[u] = __float_as_uint(32 + u < len ? -e1[u] * __uint_as_float(r1[u]) : 0.f);
+        }
+        pack64(r0, r1, pk);
+        tmem_st32(tmem_addr(tb + TM_Y, lane_base, 0), pk);
       }
-      fence_async_smem();
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&sm->y_ready);
+      if (c >= 1) epi_store();
+      // V'^T -> bf16 V'^T (columns 0-31) and V''^T = V'^T diag(e^{G_last - G}) (32-63)
+      if (!wait_wg(sm, sm->vp_full, g & 1, 0x406, kBarState)) { ok = false; break; }
+      tc_fence_after();
+      {
+        const uint32_t tu = tb + TM_U + (g & 1) * 64;
+        uint32_t r0[32], r1[32], pk[32];
+        tmem_ld32(tmem_addr(tu, lane_base, 0), r0);
+        tmem_ld32(tmem_addr(tu, lane_base, 32), r1);
+        tmem_ld_wait();
+        pack64(r0, r1, pk);
+        tmem_st32(tmem_addr(tu, lane_base, 0), pk);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float d[4];
+          ld_f4(cv.dec + q * 4, d);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) r0[q * 4 + u] = __float_as_uint(__uint_as_float(r0[q * 4 + u]) * d[u]);
+          ld_f4(cv.dec + 32 + q * 4, d);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) r1[q * 4 + u] = __float_as_uint(__uint_as_float(r1[q * 4 + u]) * d[u]);
+        }
+        pack64(r0, r1, pk);
+        tmem_st32(tmem_addr(tu, lane_base, 32), pk);
+      }
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&sm->vp_ready);
       prev_t = t;
@@ -785,7 +868,7 @@ __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
     }
     if (!ok) break;
     // end of the unit: final state, then the last chunk's output
-    if (!wait_wg(sm, sm->s_full, (g - 1) & 1, 0x406, kBarState)) break;
+    if (!wait_wg(sm, sm->s_full, (g - 1) & 1, 0x407, kBarState)) break;
     tc_fence_after();
     if (p.ht) {
 #pragma unroll 1
@@ -800,7 +883,8 @@ __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
         }
       }
     }
-    if (!epilogue(g - 1)) break;
+    if (!epi_read(g - 1)) break;
+    epi_store();
   }
 }
 
@@ -816,23 +900,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm->full[s], 2);
-      mbar_init(&sm->empty[s], 1);
+      mbar_init(&sm->empty[s], 2);  // one commit from each MMA issuer
     }
     mbar_init(&sm->x1_full, 1);
     mbar_init(&sm->x1_free, 128);
     mbar_init(&sm->t_ready, 128);
     mbar_init(&sm->uw_full, 1);
-    mbar_init(&sm->wt_ready, 128);
+    mbar_init(&sm->o1_full, 1);
     mbar_init(&sm->s_ready, 128);
+    mbar_init(&sm->y_full, 1);
+    mbar_init(&sm->y_ready, 128);
     mbar_init(&sm->vp_full, 1);
     mbar_init(&sm->vp_ready, 128);
     mbar_init(&sm->s_full, 1);
     mbar_init(&sm->o_full, 1);
     mbar_init(&sm->o_free, 128);
-    mbar_init(&sm->drain, 1);
+    mbar_init(&sm->drain, 2);
     for (int i = 0; i < kUnitRing; ++i) {
       mbar_init(&sm->unit_full[i], 1);
-      mbar_init(&sm->unit_empty[i], 1 + 128 + 128);
+      mbar_init(&sm->unit_empty[i], 2 + 128 + 128);
     }
     sm->abort = 0;
     fence_mbar_init();
@@ -862,8 +948,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     role_producer(p, sm, base, &mq, &mk, &mv);
   } else if (warp == 1) {
-    if (lane == 0) role_mma(p, sm, base);
-  } else if (warp < 6) {
+    if (lane == 0) role_issue_p(p, sm, base);
+  } else if (warp == 2) {
+    if (lane == 0) role_issue_c(p, sm, base);
+  } else if (warp < 7) {
     role_prep(p, sm, base, 32 * (warp & 3) + lane);
   } else {
     role_state(p, sm, base, 32 * (warp & 3) + lane);

@@ -85,9 +85,8 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
 // *abort becomes nonzero.  Returns true when the phase completed.  Waiting
 // threads are suspended between polls, so they do not take issue slots from
 // the warps doing the work.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
-                                          const volatile int32_t *abort, uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+__device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity,
+                                            const volatile int32_t *abort, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
@@ -96,6 +95,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
       if (globaltimer_ns() - t0 > limit_ns) return false;
     }
   }
+}
+// The polling loop is kept out of line: the kernels wait at many sites and the
+// copies would crowd the instruction cache.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          const volatile int32_t *abort, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort, limit_ns);
 }
 
 // ------------------------------------------------------------------ fences
@@ -213,6 +219,19 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]; issued by one thread.  A (M = 128 rows on the TMEM
+// lanes) holds two bf16 per 32-bit column, lower k in the low half: one K-step of 16
+// spans 8 columns.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
