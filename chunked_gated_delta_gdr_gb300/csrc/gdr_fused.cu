@@ -6,8 +6,8 @@
 // form with every intermediate on chip:
 //
 //   prep   G = cumsum(g); X1 = [K;Q] K^T (KK^T and QK^T);  A, P masks;
-//          Tm = (I + A)^-1;  Tm diag(beta) as a bf16 operand
-//   scan   Y = S^T K^T;  U^T = V^T (Tm diag(beta))^T;  V'^T = U^T - (Y diag(e^G)) (Tm diag(beta))^T
+//          Tm = (I + A)^-1;  Tm diag(beta) and Tm diag(beta e^G) as bf16 operands
+//   scan   Y = S^T K^T;  U^T = V^T (Tm diag(beta))^T;  V'^T = U^T - Y (Tm diag(beta e^G))^T
 //          (so V' = U - W S with W = Tm diag(beta e^G) K, never formed);
 //          S^T <- e^{G_last} S^T + V''^T K,  V'' = diag(e^{G_last-G}) V'
 //   out    O^T = e^G-scaled S^T Q^T + V'^T P^T,  P_ij = e^{G_i-G_j} q_i.k_j (j <= i)
@@ -58,7 +58,8 @@ constexpr uint32_t kStageBytes = kKQBytes + kVBytes;
 constexpr uint32_t OFF_STAGE = 0;
 constexpr uint32_t OFF_P = OFF_STAGE + kStages * kStageBytes;  // P bf16, 2 buffers of 64 x 64
 constexpr uint32_t OFF_TB = OFF_P + 16384;     // Tm diag(beta) bf16 64 x 64
-constexpr uint32_t OFF_STG = OFF_TB + 8192;    // output staging [64 tokens][128 dv] bf16
+constexpr uint32_t OFF_TBG = OFF_TB + 8192;    // -Tm diag(beta e^G) bf16 64 x 64
+constexpr uint32_t OFF_STG = OFF_TBG + 8192;   // output staging [64 tokens][128 dv] bf16
 constexpr uint32_t OFF_A = OFF_STG + 16384;    // solve scratch fp32 64 x kLdA
 constexpr uint32_t OFF_Y = OFF_A + 17408;      // solve scratch fp32 32 x kLdY
 constexpr uint32_t OFF_SMALL = OFF_Y + 5120;
@@ -72,7 +73,7 @@ constexpr uint32_t TM_S = 0;     // S^T fp32, 128 columns (key dim)
 constexpr uint32_t TM_SB = 128;  // S^T bf16 pairs (A operand), 64 columns
 constexpr uint32_t TM_U = 192;   // two buffers of 64 columns, by chunk parity: X1, then U^T ->
                                  // V'^T fp32, then bf16 V'^T (cols 0-31) and V''^T (32-63)
-constexpr uint32_t TM_Y = 320;   // Y = S^T K^T fp32, then -Y diag(e^G) as bf16 pairs in cols 0-31
+constexpr uint32_t TM_Y = 320;   // Y = S^T K^T fp32, then bf16 pairs in cols 0-31
 constexpr uint32_t TM_O = 384;   // S^T Q^T (inter-chunk part of O^T), 64 columns
 constexpr uint32_t TM_O2 = 448;  // V'^T P^T (intra-chunk part of O^T), 64 columns
 constexpr uint32_t kTmemCols = 512;
@@ -333,12 +334,22 @@ __device__ void issuer_drain(Small *sm) {
   mbar_wait(&sm->drain, 0, nullptr, kWaitLimitNs);
 }
 
+// A shared-memory descriptor moved by `bytes` (a multiple of 16; the address field
+// does not overflow inside the 227 KB window).
+__device__ __forceinline__ uint64_t dadd(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
 __device__ void role_issue_p(const Params &p, Small *sm, uint8_t *base) {
   const uint32_t tb = sm->tmem_base;
   const uint32_t sbase = smem_u32(base);
   const uint32_t id_x1 = idesc_bf16(128, 64, false, false);
   const uint32_t id_uw = idesc_bf16(128, 64, true, false);  // A = V^T (MN-major)
   const uint32_t id_n64 = idesc_bf16(128, 64, false, false);
+  // descriptors of stage 0 / buffer 0; stages are kStageBytes apart
+  const uint64_t d_kq = sdesc_sw128(sbase + OFF_STAGE, 0, 1024);          // K rows (K-major)
+  const uint64_t d_q = sdesc_sw128(sbase + OFF_STAGE + 8192, 0, 1024);    // Q rows (K-major)
+  const uint64_t d_v = sdesc_sw128(sbase + OFF_STAGE + kKQBytes, 8192, 1024);  // V (MN-major)
+  const uint64_t d_tb = sdesc_sw128(sbase + OFF_TB, 0, 1024);
+  const uint64_t d_p = sdesc_sw128(sbase + OFF_P, 0, 1024);
   uint32_t g = 0;
   bool ok = true;
   // X1 of chunk gg into its U buffer (by parity).  It needs its stage, prep done
@@ -354,12 +365,12 @@ __device__ void role_issue_p(const Params &p, Small *sm, uint8_t *base) {
     return true;
   };
   auto issue_x1 = [&](uint32_t gg) {
-    const uint32_t kq = sbase + OFF_STAGE + (gg % kStages) * kStageBytes;
+    const uint64_t a = dadd(d_kq, (gg % kStages) * kStageBytes);
     const uint32_t d = tb + TM_U + (gg & 1) * 64;
 #pragma unroll 1
     for (int kk = 0; kk < 8; ++kk) {
-      const uint32_t a = kq + (kk / 4) * 16384 + (kk % 4) * 32;
-      mma_bf16(d, sdesc_sw128(a, 0, 1024), sdesc_sw128(a, 0, 1024), id_x1, kk > 0);
+      const uint64_t ak = dadd(a, (kk / 4) * 16384 + (kk % 4) * 32);
+      mma_bf16(d, ak, ak, id_x1, kk > 0);
     }
     mma_commit(&sm->x1_full);
   };
@@ -371,8 +382,6 @@ __device__ void role_issue_p(const Params &p, Small *sm, uint8_t *base) {
     if (ui.seq < 0) break;
     for (int c = 0; c < ui.nch; ++c, ++g) {
       const uint32_t s = g % kStages;
-      const uint32_t kq = sbase + OFF_STAGE + s * kStageBytes;
-      const uint32_t vv = kq + kKQBytes;
       const uint32_t tu = tb + TM_U + (g & 1) * 64;
       if (c == 0) {
         if (!x1_wait(g, 0x202)) { ok = false; break; }
@@ -386,29 +395,34 @@ __device__ void role_issue_p(const Params &p, Small *sm, uint8_t *base) {
       // U^T = V^T (Tm diag beta)^T
       if (!wait1(sm, sm->t_ready, g & 1, 0x208)) { ok = false; break; }
       tc_fence_after();
+      {
+        const uint64_t dv = dadd(d_v, s * kStageBytes);
 #pragma unroll 1
-      for (int kk = 0; kk < 4; ++kk)
-        mma_bf16(tu, sdesc_sw128(vv + kk * 2048, 8192, 1024),
-                 sdesc_sw128(sbase + OFF_TB + kk * 32, 0, 1024), id_uw, kk > 0);
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16(tu, dadd(dv, kk * 2048), dadd(d_tb, kk * 32), id_uw, kk > 0);
+      }
       mma_commit(&sm->uw_full);
       // O^T (inter-chunk part) = S^T Q^T, once the epilogue has read the previous chunk's
       if (!wait1(sm, sm->s_ready, g & 1, 0x209)) { ok = false; break; }
       if (g >= 1 && !wait1(sm, sm->o_free, (g - 1) & 1, 0x20a)) { ok = false; break; }
       tc_fence_after();
+      {
+        const uint64_t dq = dadd(d_q, s * kStageBytes);
 #pragma unroll 1
-      for (int kk = 0; kk < 8; ++kk)
-        mma_bf16_ts(tb + TM_O, tb + TM_SB + kk * 8,
-                    sdesc_sw128(kq + (kk / 4) * 16384 + 8192 + (kk % 4) * 32, 0, 1024), id_n64,
-                    kk > 0);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ts(tb + TM_O, tb + TM_SB + kk * 8, dadd(dq, (kk / 4) * 16384 + (kk % 4) * 32),
+                      id_n64, kk > 0);
+      }
       mma_commit(&sm->o1_full);  // the bf16 copy of S^T is free as far as O1 goes
       // O2^T = V'^T P^T
       if (!wait1(sm, sm->vp_ready, g & 1, 0x20b)) { ok = false; break; }
       tc_fence_after();
+      {
+        const uint64_t dp = dadd(d_p, (g & 1) * 8192);
 #pragma unroll 1
-      for (int kk = 0; kk < 4; ++kk)
-        mma_bf16_ts(tb + TM_O2, tu + kk * 8,
-                    sdesc_sw128(sbase + OFF_P + (g & 1) * 8192 + kk * 32, 0, 1024), id_n64,
-                    kk > 0);
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16_ts(tb + TM_O2, tu + kk * 8, dadd(dp, kk * 32), id_n64, kk > 0);
+      }
       mma_commit(&sm->o_full);
       mma_commit(&sm->empty[s]);
     }
@@ -421,6 +435,9 @@ __device__ void role_issue_c(const Params &p, Small *sm, uint8_t *base) {
   const uint32_t sbase = smem_u32(base);
   const uint32_t id_n64 = idesc_bf16(128, 64, false, false);
   const uint32_t id_su = idesc_bf16(128, 128, false, true);  // B = K (MN-major)
+  const uint64_t d_k = sdesc_sw128(sbase + OFF_STAGE, 0, 1024);        // K rows (K-major)
+  const uint64_t d_kmn = sdesc_sw128(sbase + OFF_STAGE, 16384, 1024);  // K (MN-major)
+  const uint64_t d_tbg = sdesc_sw128(sbase + OFF_TBG, 0, 1024);
   uint32_t g = 0;
   bool ok = true;
   for (uint32_t k = 0; ok; ++k) {
@@ -431,32 +448,30 @@ __device__ void role_issue_c(const Params &p, Small *sm, uint8_t *base) {
     if (ui.seq < 0) break;
     for (int c = 0; c < ui.nch; ++c, ++g) {
       const uint32_t s = g % kStages;
-      const uint32_t kq = sbase + OFF_STAGE + s * kStageBytes;
       const uint32_t tu = tb + TM_U + (g & 1) * 64;
+      const uint64_t dk = dadd(d_k, s * kStageBytes), dkmn = dadd(d_kmn, s * kStageBytes);
       // Y = S^T K^T  (S before this chunk, bf16 in TMEM)
       if (!wait1(sm, sm->s_ready, g & 1, 0x212)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll 1
       for (int kk = 0; kk < 8; ++kk)
-        mma_bf16_ts(tb + TM_Y, tb + TM_SB + kk * 8,
-                    sdesc_sw128(kq + (kk / 4) * 16384 + (kk % 4) * 32, 0, 1024), id_n64, kk > 0);
+        mma_bf16_ts(tb + TM_Y, tb + TM_SB + kk * 8, dadd(dk, (kk / 4) * 16384 + (kk % 4) * 32),
+                    id_n64, kk > 0);
       mma_commit(&sm->y_full);
-      // V'^T = U^T + (-Y diag(e^G)) (Tm diag(beta))^T
+      // V'^T = U^T + Y (-Tm diag(beta e^G))^T
       if (!wait1(sm, sm->y_ready, g & 1, 0x213)) { ok = false; break; }
       if (!wait1(sm, sm->uw_full, g & 1, 0x214)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll 1
       for (int kk = 0; kk < 4; ++kk)
-        mma_bf16_ts(tu, tb + TM_Y + kk * 8, sdesc_sw128(sbase + OFF_TB + kk * 32, 0, 1024),
-                    id_n64, 1);
+        mma_bf16_ts(tu, tb + TM_Y + kk * 8, dadd(d_tbg, kk * 32), id_n64, 1);
       mma_commit(&sm->vp_full);
       // S^T += V''^T K
       if (!wait1(sm, sm->vp_ready, g & 1, 0x215)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll 1
       for (int kk = 0; kk < 4; ++kk)
-        mma_bf16_ts(tb + TM_S, tu + 32 + kk * 8, sdesc_sw128(kq + kk * 2048, 16384, 1024), id_su,
-                    1);
+        mma_bf16_ts(tb + TM_S, tu + 32 + kk * 8, dadd(dkmn, kk * 2048), id_su, 1);
       mma_commit(&sm->s_full);
       mma_commit(&sm->empty[s]);
     }
@@ -658,8 +673,8 @@ __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
         warp_store16(AS + (32 + 16 * mt) * kLdA + 16 * nt, kLdA, acc2, -1.f);
       }
       named_bar(kBarPrep, 128);
-      // Tm diag(beta) as a bf16 operand, half a row per thread, once the previous
-      // chunk's MMAs that read it are done
+      // Tm diag(beta) and -Tm diag(beta e^G) as bf16 operands, half a row per thread,
+      // once the previous chunk's MMAs that read them are done
       {
         const int ri = pid & 63, hc = (pid >> 6) * 32;
         float v[32];
@@ -674,6 +689,15 @@ __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
         if (g >= 1 && !wait_wg(sm, sm->vp_full, (g - 1) & 1, 0x305, kBarPrep)) { ok = false; break; }
 #pragma unroll
         for (int q = 0; q < 4; ++q) store_chunk8(sbase + OFF_TB, ri, hc + q * 8, v + q * 8);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float eq[4];
+          ld_f4(cv.eG + hc + q * 4, eq);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) v[q * 4 + u] *= -eq[u];
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) store_chunk8(sbase + OFF_TBG, ri, hc + q * 8, v + q * 8);
       }
       fence_async_smem();
       mbar_arrive(&sm->t_ready);
@@ -808,25 +832,21 @@ __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
       mbar_arrive(&sm->s_ready);
       // previous chunk's output accumulators (same unit) -> staging, while Y is computed
       if (c >= 1 && !epi_read(g - 1)) { ok = false; break; }
-      // -Y diag(e^G) -> bf16 pairs in place; token columns past the chunk's end are
-      // zeroed so that whatever the stage holds there cannot reach V'
+      // Y -> bf16 pairs in place; token columns past the chunk's end are zeroed so that
+      // whatever the stage holds there cannot reach V'
       if (!wait_wg(sm, sm->y_full, g & 1, 0x405, kBarState)) { ok = false; break; }
       tc_fence_after();
       {
         uint32_t r0[32], r1[32], pk[32];
         tmem_ld32(tmem_addr(tb + TM_Y, lane_base, 0), r0);
         tmem_ld32(tmem_addr(tb + TM_Y, lane_base, 32), r1);
-        float e0[32], e1[32];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          ld_f4(cv.eG + q * 4, e0 + q * 4);
-          ld_f4(cv.eG + 32 + q * 4, e1 + q * 4);
-        }
         tmem_ld_wait();
+        if (len < kChunk) {
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          r0[u] = __float_as_uint(u < len ? -e0[u] * __uint_as_float(r0[u]) : 0.f);
-          r1[u] = __float_as_uint(32 + u < len ? -e1[u] * __uint_as_float(r1[u]) : 0.f);
+          for (int u = 0; u < 32; ++u) {
+            if (u >= len) r0[u] = 0u;
+            if (32 + u >= len) r1[u] = 0u;
+          }
         }
         pack64(r0, r1, pk);
         tmem_st32(tmem_addr(tb + TM_Y, lane_base, 0), pk);
