@@ -553,8 +553,19 @@ __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
       const int len = min(kChunk, ui.end - t);
       const uint32_t kq_a = sbase + OFF_STAGE + s * kStageBytes;
       const int cb2 = g & 1;
-      if (!wait_wg(sm, sm->full[s], (g / kStages) & 1, 0x302, kBarPrep)) { ok = false; break; }
-      // zero the rows past the chunk's end (they hold the next segment's tokens)
+      // the chunk's stage and X1 (one barrier for both waits)
+      {
+        const bool bad = !mbar_wait(&sm->full[s], (g / kStages) & 1, &sm->abort, kWaitLimitNs) ||
+                         !mbar_wait(&sm->x1_full, g & 1, &sm->abort, kWaitLimitNs);
+        if (named_bar_or(kBarPrep, 128, bad)) {
+          fail(sm, 0x302);
+          ok = false;
+          break;
+        }
+      }
+      tc_fence_after();
+      // zero the rows past the chunk's end (they hold the next segment's tokens); the
+      // MMAs that read them before this (X1, Y, O1) only feed masked or unstored values
       if (len < kChunk) {
         for (int idx = pid; idx < (kChunk - len) * 6; idx += 128) {
           const int r = len + idx / 6, which = idx % 6;
@@ -570,8 +581,6 @@ __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
       }
       const ChunkVec &cv = sm->cv[g % kInfo];
       // X1 rows: lanes 0-63 = K K^T (rows of A), lanes 64-127 = Q K^T (rows of P)
-      if (!wait_wg(sm, sm->x1_full, g & 1, 0x303, kBarPrep)) { ok = false; break; }
-      tc_fence_after();
       {
         // A_ij = beta_i e^{G_i-G_j} k_i.k_j (j < i);  P_ij = scale e^{G_i-G_j} q_i.k_j (j <= i)
         const int i = row & 63;
@@ -636,7 +645,7 @@ __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
             x[r] = s0 + s1;
           }
         }
-        named_bar(kBarPrep, 128);
+        __syncwarp();  // a block's 16 columns belong to one warp
         if (pid < 64) {
 #pragma unroll
           for (int r = 0; r < 16; ++r) blk[r * kLdA + cc] = x[r];
@@ -651,12 +660,10 @@ __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
           float acc[2][4] = {};
           warp_mm16(AS + oa * kLdA + ob, kLdA, AS + ob * kLdA + ob, kLdA, 16, acc);
           warp_store16(X, kLdX, acc, 1.f);
-        }
-        named_bar(kBarPrep, 128);
-        if (wq < 2) {
-          float acc[2][4] = {};
-          warp_mm16(AS + oa * kLdA + oa, kLdA, X, kLdX, 16, acc);
-          warp_store16(AS + oa * kLdA + ob, kLdA, acc, -1.f);
+          __syncwarp();  // X is this warp's own scratch
+          float acc2[2][4] = {};
+          warp_mm16(AS + oa * kLdA + oa, kLdA, X, kLdX, 16, acc2);
+          warp_store16(AS + oa * kLdA + ob, kLdA, acc2, -1.f);
         }
       }
       named_bar(kBarPrep, 128);
@@ -669,7 +676,8 @@ __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
         named_bar(kBarPrep, 128);
         float acc2[2][4] = {};
         warp_mm16(AS + (32 + 16 * mt) * kLdA + 32, kLdA, YS + 16 * nt, kLdY, 32, acc2);
-        named_bar(kBarPrep, 128);
+        // the result overwrites A[32:64, 0:32], which every warp finished reading before
+        // the barrier above
         warp_store16(AS + (32 + 16 * mt) * kLdA + 16 * nt, kLdA, acc2, -1.f);
       }
       named_bar(kBarPrep, 128);
