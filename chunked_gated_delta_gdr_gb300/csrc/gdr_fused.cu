@@ -626,30 +626,37 @@ __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
       named_bar(kBarPrep, 128);
       // ---- Tm = (I + A)^-1, 64 x 64 unit lower triangular, fp32 ----
       // phase 1: the four 16 x 16 diagonal blocks by forward substitution, one
-      // column per thread (threads 0..63)
-      {
+      // column per thread (threads 0..63; a block's 16 threads share a warp); the next
+      // row's entries are loaded while the current row is solved
+      if (pid < 64) {
         const int b = (pid >> 4) & 3, cc = pid & 15;
         float *blk = AS + 16 * b * kLdA + 16 * b;
         float x[16];
-        if (pid < 64) {
+        float an[16];  // entries m < r of the next row r
 #pragma unroll
-          for (int r = 0; r < 16; ++r) {
-            float a[16];
+        for (int m = 0; m < 16; ++m) an[m] = 0.f;
+        an[0] = blk[1 * kLdA];
+        x[0] = (cc == 0) ? 1.f : 0.f;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) ld_f4(blk + r * kLdA + q * 4, a + q * 4);
-            float s0 = (r == cc) ? 1.f : 0.f, s1 = 0.f;
+        for (int r = 1; r < 16; ++r) {
+          float a[16];
 #pragma unroll
-            for (int m = 0; m < r; ++m) {
-              if (m & 1) s1 -= a[m] * x[m]; else s0 -= a[m] * x[m];
-            }
-            x[r] = s0 + s1;
+          for (int m = 0; m < 16; ++m) a[m] = an[m];
+          if (r + 1 < 16) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (q * 4 < r + 1) ld_f4(blk + (r + 1) * kLdA + q * 4, an + q * 4);
           }
-        }
-        __syncwarp();  // a block's 16 columns belong to one warp
-        if (pid < 64) {
+          float s0 = (r == cc) ? 1.f : 0.f, s1 = 0.f;
 #pragma unroll
-          for (int r = 0; r < 16; ++r) blk[r * kLdA + cc] = x[r];
+          for (int m = 0; m < r; ++m) {
+            if (m & 1) s1 -= a[m] * x[m]; else s0 -= a[m] * x[m];
+          }
+          x[r] = s0 + s1;
         }
+        __syncwarp();
+#pragma unroll
+        for (int r = 0; r < 16; ++r) blk[r * kLdA + cc] = x[r];
       }
       named_bar(kBarPrep, 128);
       // phase 2: T_{b+1,b} = -D_{b+1} A_{b+1,b} D_b for b = 0, 2 (warps 0 and 1)
