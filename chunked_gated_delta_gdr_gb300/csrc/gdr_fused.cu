@@ -582,18 +582,35 @@ __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
       const ChunkVec &cv = sm->cv[g % kInfo];
       // X1 rows: lanes 0-63 = K K^T (rows of A), lanes 64-127 = Q K^T (rows of P)
       {
-        // A_ij = beta_i e^{G_i-G_j} k_i.k_j (j < i);  P_ij = scale e^{G_i-G_j} q_i.k_j (j <= i)
+        // A_ij = beta_i e^{G_i-G_j} k_i.k_j (j < i);  P_ij = scale e^{G_i-G_j} q_i.k_j (j <= i).
+        // Only what the solve and the O2 MMA read is masked: A's entries on and above the
+        // diagonal are never read except the two 16 x 16 blocks inside the 32 x 32
+        // diagonal blocks (rows 0-15 / 32-47, the next 16 columns), which must be zero;
+        // P is an MMA operand, so all its entries above the diagonal must be zero.  Rows
+        // past the chunk's end are zero (ci = 0).  Per 32-column half, the warp's rows
+        // (one lane quadrant) lie either below, on or above the half's diagonal block.
         const int i = row & 63;
-        const bool live = i < len;
         const bool is_a = row < 64;
+        const bool upper = i < 32;  // same for the whole warp
         const float scl = is_a ? cv.beta[i] : p.scale;
-        const int lim = is_a ? i : i + 1;
         const bool fac = cv.fac != 0;  // same for the whole chunk
         const float gi = cv.G[i];
-        const float ci = fac ? scl * ex2(gi - cv.Gref) : scl;
+        const float ci = i < len ? (fac ? scl * ex2(gi - cv.Gref) : scl) : 0.f;
         const uint32_t tx1 = tb + TM_U + (g & 1) * 64;
+        const uint32_t ptile = sbase + OFF_P + cb2 * 8192;
+        // kept columns u (within the diagonal half) satisfy u <= keep
+        const int keep = is_a ? (((i & 31) < 16) ? 15 : 31) : (i & 31);
 #pragma unroll 1
         for (int hh = 0; hh < 2; ++hh) {  // 32 columns at a time
+          if (hh == 1 && upper) {  // above the diagonal: A is never read there, P is zero
+            if (!is_a) {
+              const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+              for (int q = 0; q < 4; ++q) store_chunk8(ptile, i, 32 + q * 8, z);
+            }
+            continue;
+          }
+          const int lim = (hh == 0) == upper ? keep : 31;  // diagonal half or fully below
           uint32_t r[32];
           tmem_ld32(tmem_addr(tx1, lane_base, hh * 32), r);
           float f[32];
@@ -604,20 +621,17 @@ __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
             for (int u = 0; u < 32; ++u) f[u] = ex2(gi - f[u]);
           }
           tmem_ld_wait();
-          float v[32];
 #pragma unroll
           for (int u = 0; u < 32; ++u) {
-            const int j = hh * 32 + u;
             const float prod = (ci * f[u]) * __uint_as_float(r[u]);
-            v[u] = (live && j < lim) ? prod : 0.f;
+            f[u] = u <= lim ? prod : 0.f;
           }
           if (is_a) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) st_f4(AS + i * kLdA + hh * 32 + q * 4, v + q * 4);
+            for (int q = 0; q < 8; ++q) st_f4(AS + i * kLdA + hh * 32 + q * 4, f + q * 4);
           } else {
-            const uint32_t ptile = sbase + OFF_P + cb2 * 8192;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) store_chunk8(ptile, i, hh * 32 + q * 8, v + q * 8);
+            for (int q = 0; q < 4; ++q) store_chunk8(ptile, i, hh * 32 + q * 8, f + q * 8);
           }
         }
       }
