@@ -62,6 +62,11 @@ def open_library(path: str):
         ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
         ctypes.c_int32, ctypes.c_int32, vp, vp, ci]
     lib.gdr_oracle_recurrent.restype = ci
+    lib.gdr_oracle_recurrent_ckpt.argtypes = [
+        vp, ci, vp, ci, vp, ci, vp, ci, vp, ci, cd, vp, ci, vp,
+        ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+        ctypes.c_int32, ctypes.c_int32, vp, vp, ctypes.c_int32, vp, vp, ci]
+    lib.gdr_oracle_recurrent_ckpt.restype = ci
     lib.gdr_oracle_max_threads.restype = ci
     return lib
 
@@ -136,3 +141,43 @@ def recurrent(q, k, v, g, beta, scale, h0, cu_seqlens, want_ht=True,
     if rc != 0:
         raise RuntimeError(f"gdr_oracle_recurrent failed with code {rc}")
     return o, ht
+
+
+def recurrent_checkpoints(q, k, v, g, beta, scale, h0, cu_seqlens, ckpt_every, want_ht=True,
+                          o_init=np.nan, n_threads=0, lib=None):
+    """``recurrent`` plus state checkpoints every ``ckpt_every`` tokens of each segment.
+
+    Returns (o, ht, ckpt [rows, H, dk, dv] float64, ckpt_off [N + 1] int32): checkpoint m
+    (1-based) of segment n is row ckpt_off[n] + m - 1, the state after the segment's first
+    m * ckpt_every tokens.
+    """
+    lib = _load() if lib is None else lib
+    qa, qd = _as_np(q)
+    ka, kd = _as_np(k)
+    va, vd = _as_np(v)
+    ga, gd = _as_np(g)
+    ba, bd = _as_np(beta)
+    ha, hd = _as_np(h0)
+    try:
+        import torch
+        if isinstance(cu_seqlens, torch.Tensor):
+            cu_seqlens = cu_seqlens.cpu().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    T, Hk, dk = qa.shape
+    H, dv = va.shape[1], va.shape[2]
+    n_seq = cu.shape[0] - 1
+    o = np.full((T, H, dv), o_init, dtype=np.float64)
+    ht = np.zeros((n_seq, H, dk, dv), dtype=np.float64) if want_ht else None
+    rows = max(T // int(ckpt_every), 1)
+    ckpt = np.zeros((rows, H, dk, dv), dtype=np.float64)
+    off = np.zeros(n_seq + 1, dtype=np.int32)
+    ptr = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+    rc = lib.gdr_oracle_recurrent_ckpt(
+        ptr(qa), qd, ptr(ka), kd, ptr(va), vd, ptr(ga), gd, ptr(ba), bd,
+        float(scale), ptr(ha), hd, ptr(cu), n_seq, T, Hk, H, dk, dv,
+        ptr(o), ptr(ht), int(ckpt_every), ptr(ckpt), ptr(off), int(n_threads))
+    if rc != 0:
+        raise RuntimeError(f"gdr_oracle_recurrent_ckpt failed with code {rc}")
+    return o, ht, ckpt[:off[-1]], off

@@ -31,6 +31,15 @@
  *
  * Grouped heads: value head h reads query/key head h / (H / Hk).
  *
+ * State checkpoints (gdr_oracle_recurrent_ckpt): every `ckpt_every` tokens of a
+ * segment the state is copied out, as for prefix caching ("feat(cake_kda): add
+ * paired recurrent training for SM100a and SM103a", the released inference
+ * surface keeps state checkpoints every N tokens).  Checkpoint m (m = 1, 2, ...,
+ * floor(len / ckpt_every)) of segment n is S after the segment's first
+ * m * ckpt_every tokens; segment n's checkpoints fill rows ckpt_off[n] ..
+ * ckpt_off[n + 1] - 1 of ckpt[rows, H, dk, dv], ckpt_off being the running sum
+ * of floor(len / ckpt_every).
+ *
  * Inputs are read in their stored precision (bf16 bits, fp32 or fp64) and
  * promoted exactly to double.  Outputs are double.
  */
@@ -69,13 +78,14 @@ static void orc_bounds(const int32_t *cu, int32_t n, int64_t T, int64_t *s, int6
   *e = prev;
 }
 
-int gdr_oracle_recurrent(const void *q, int q_dt, const void *k, int k_dt,
-                         const void *v, int v_dt, const void *g, int g_dt,
-                         const void *beta, int beta_dt, double scale,
-                         const void *h0, int h0_dt, const int32_t *cu_seqlens,
-                         int32_t n_seq, int64_t T, int32_t Hk, int32_t H,
-                         int32_t dk, int32_t dv, double *o, double *ht,
-                         int n_threads) {
+static int orc_run(const void *q, int q_dt, const void *k, int k_dt,
+                   const void *v, int v_dt, const void *g, int g_dt,
+                   const void *beta, int beta_dt, double scale,
+                   const void *h0, int h0_dt, const int32_t *cu_seqlens,
+                   int32_t n_seq, int64_t T, int32_t Hk, int32_t H,
+                   int32_t dk, int32_t dv, double *o, double *ht,
+                   int32_t ckpt_every, double *ckpt, const int32_t *ckpt_off,
+                   int n_threads) {
   if (!q || !k || !v || !g || !beta || !cu_seqlens || !o) return -1;
   if (n_seq < 0 || T < 0 || Hk <= 0 || H <= 0 || dk <= 0 || dv <= 0) return -2;
   if (H % Hk != 0) return -3;
@@ -143,6 +153,11 @@ int gdr_oracle_recurrent(const void *q, int q_dt, const void *k, int k_dt,
             for (int32_t j = 0; j < dv; ++j) ot[j] += row[j] * qi;
           }
           for (int32_t j = 0; j < dv; ++j) ot[j] *= scale;
+          /* state checkpoint after the segment's first m * ckpt_every tokens */
+          if (ckpt && (t - s + 1) % ckpt_every == 0) {
+            const int64_t row = ckpt_off[n] + (t - s + 1) / ckpt_every - 1;
+            memcpy(ckpt + (row * H + h) * dk * dv, S, sizeof(double) * (size_t)dk * dv);
+          }
         }
         if (ht) memcpy(ht + ((int64_t)n * H + h) * dk * dv, S, sizeof(double) * (size_t)dk * dv);
       }
@@ -154,6 +169,39 @@ int gdr_oracle_recurrent(const void *q, int q_dt, const void *k, int k_dt,
     free(qv);
   }
   return bad ? -4 : 0;
+}
+
+int gdr_oracle_recurrent(const void *q, int q_dt, const void *k, int k_dt,
+                         const void *v, int v_dt, const void *g, int g_dt,
+                         const void *beta, int beta_dt, double scale,
+                         const void *h0, int h0_dt, const int32_t *cu_seqlens,
+                         int32_t n_seq, int64_t T, int32_t Hk, int32_t H,
+                         int32_t dk, int32_t dv, double *o, double *ht,
+                         int n_threads) {
+  return orc_run(q, q_dt, k, k_dt, v, v_dt, g, g_dt, beta, beta_dt, scale, h0, h0_dt,
+                 cu_seqlens, n_seq, T, Hk, H, dk, dv, o, ht, 0, NULL, NULL, n_threads);
+}
+
+/* As gdr_oracle_recurrent, plus state checkpoints (see the header comment).
+ * ckpt_off [n_seq + 1] is written here; ckpt needs ckpt_off[n_seq] rows. */
+int gdr_oracle_recurrent_ckpt(const void *q, int q_dt, const void *k, int k_dt,
+                              const void *v, int v_dt, const void *g, int g_dt,
+                              const void *beta, int beta_dt, double scale,
+                              const void *h0, int h0_dt, const int32_t *cu_seqlens,
+                              int32_t n_seq, int64_t T, int32_t Hk, int32_t H,
+                              int32_t dk, int32_t dv, double *o, double *ht,
+                              int32_t ckpt_every, double *ckpt, int32_t *ckpt_off,
+                              int n_threads) {
+  if (ckpt_every <= 0 || !ckpt || !ckpt_off || !cu_seqlens || n_seq < 0) return -5;
+  ckpt_off[0] = 0;
+  for (int32_t n = 0; n < n_seq; ++n) {
+    int64_t s, e;
+    orc_bounds(cu_seqlens, n, T, &s, &e);
+    ckpt_off[n + 1] = ckpt_off[n] + (int32_t)((e - s) / ckpt_every);
+  }
+  return orc_run(q, q_dt, k, k_dt, v, v_dt, g, g_dt, beta, beta_dt, scale, h0, h0_dt,
+                 cu_seqlens, n_seq, T, Hk, H, dk, dv, o, ht, ckpt_every, ckpt, ckpt_off,
+                 n_threads);
 }
 
 int gdr_oracle_max_threads(void) {

@@ -246,9 +246,50 @@ def pin_bf16_decoding(rec):
     assert np.array_equal(o1, o2) and np.array_equal(h1, h2)
 
 
+def _ckpt(rec, d, every):
+    """State checkpoints from the oracle library ``rec`` runs on (mutants included)."""
+    lib = getattr(rec, "keywords", {}).get("lib")
+    return oracle.recurrent_checkpoints(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"],
+                                        d["h0"], d["cu"], every, lib=lib)
+
+
+def pin_checkpoint_prefixes(rec):
+    # checkpoint m of a segment is the final state of the segment cut after m * every
+    # tokens (the checkpoint feature of "feat(cake_kda): add paired recurrent training for
+    # SM100a and SM103a", kept inference surface); the offsets are the running sum of
+    # floor(len / every)
+    lens, every = [150, 0, 128, 200, 3], 64
+    d = _random_f64(101, lens, 1, 2, 5, 4)
+    o, ht, ck, off = _ckpt(rec, d, every)
+    assert off.tolist() == [0, 2, 2, 4, 7, 7]
+    o2, ht2 = _run(rec, d)
+    assert np.array_equal(o, o2) and np.array_equal(ht, ht2)
+    starts = d["cu"][:-1]
+    for n, L in enumerate(lens):
+        for m in range(1, L // every + 1):
+            dn = dict(d, cu=np.array([starts[n], starts[n] + m * every], dtype=np.int32),
+                      h0=d["h0"][n:n + 1])
+            _, hp = _run(rec, dn)
+            assert np.array_equal(ck[off[n] + m - 1], hp[0]), (n, m)
+
+
+def pin_checkpoint_resume(rec):
+    # resuming from a checkpoint reproduces the rest of the segment
+    d = _random_f64(111, [300], 2, 2, 4, 4)
+    o, ht, ck, off = _ckpt(rec, d, 128)
+    assert off.tolist() == [0, 2]
+    for m in (1, 2):
+        cut = 128 * m
+        d2 = dict(d, cu=np.array([cut, 300], dtype=np.int32), h0=ck[m - 1:m])
+        o2, h2 = _run(rec, d2)
+        np.testing.assert_allclose(o2[cut:], o[cut:], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(h2[0], ht[0], rtol=0, atol=1e-12)
+
+
 PINS = [pin_hand_worked, pin_chunked_form, pin_unrolled_products, pin_beta_zero,
         pin_overwrite, pin_single_token, pin_ghosts, pin_chaining, pin_grouped_heads,
-        pin_linearity, pin_segment_reading, pin_bf16_decoding]
+        pin_linearity, pin_segment_reading, pin_bf16_decoding, pin_checkpoint_prefixes,
+        pin_checkpoint_resume]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -304,6 +345,10 @@ MUTATIONS = {
     "h0_head_index": ("((int64_t)n * H + h) * dk * dv + i", "((int64_t)h * n_seq + n) * dk * dv + i"),
     "bf16_decode_shift": ("<< 16;", "<< 15;"),
     "segment_running_max": ("if (i > 0 && c < prev) c = prev;", ""),
+    "checkpoint_segment_offset": ("const int64_t row = ckpt_off[n] +",
+                                  "const int64_t row = ckpt_off[0] +"),
+    "checkpoint_at_segment_end": ("(t - s + 1) % ckpt_every == 0",
+                                  "(t - s + 1) % ckpt_every == 0 && t + 1 < e"),
 }
 
 
