@@ -6,9 +6,11 @@ first call does, and raises if the library has not been built.
 """
 from .api import (  # noqa: F401
     check_cu_seqlens,
+    checkpoint_count_bound,
     chunk_count_bound,
     chunk_fwd,
     chunk_fwd_alloc,
+    chunk_fwd_checkpoints,
     chunk_index,
     chunk_out,
     chunk_prep,

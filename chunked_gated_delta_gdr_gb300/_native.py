@@ -15,7 +15,7 @@ STATUS = {
     0: "GDR_OK", -1: "GDR_ERR_NULL", -2: "GDR_ERR_DTYPE", -3: "GDR_ERR_SHAPE",
     -4: "GDR_ERR_STRIDE", -5: "GDR_ERR_DIM", -6: "GDR_ERR_HEADS", -7: "GDR_ERR_NSEQ",
     -8: "GDR_ERR_WORKSPACE", -9: "GDR_ERR_PATH", -10: "GDR_ERR_CUDA", -11: "GDR_ERR_ALIGN",
-    -12: "GDR_ERR_DEVICE", -13: "GDR_ERR_SCRATCH_LIMIT",
+    -12: "GDR_ERR_DEVICE", -13: "GDR_ERR_SCRATCH_LIMIT", -14: "GDR_ERR_CKPT",
 }
 
 # Every function the header declares, with its ctypes signature.
@@ -35,6 +35,9 @@ SIGNATURES = {
     "gdr_chunk_fwd_workspace_bytes": (_sz, [_i64, _i32, _i32, _i32, _i32, _i32]),
     "gdr_chunk_fwd_ws": (ctypes.c_int, [_T, _T, _T, _T, _T, _f32, _T, _vp, _i32, _T, _T, _i32,
                                         _vp, _sz, _vp]),
+    "gdr_chunk_fwd_ckpt": (ctypes.c_int, [_T, _T, _T, _T, _T, _f32, _T, _vp, _i32, _T, _T, _T,
+                                          _vp, _i32, _i32, _vp, _sz, _vp]),
+    "gdr_ckpt_count_bound": (_i64, [_i64, _i32]),
     "gdr_chunk_count_bound": (_i64, [_i64, _i32]),
     "gdr_stage_workspace_bytes": (_sz, [_i64, _i32]),
     "gdr_chunk_index": (ctypes.c_int, [_vp, _i32, _i64, _vp, _vp, _vp, _vp]),

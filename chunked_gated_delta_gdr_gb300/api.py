@@ -127,6 +127,47 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor
     return o, ht
 
 
+def checkpoint_count_bound(T: int, checkpoint_every_n_tokens: int) -> int:
+    """Rows ``chunk_fwd_checkpoints`` may write: floor(T / checkpoint_every_n_tokens)."""
+    return int(nat.lib().gdr_ckpt_count_bound(T, checkpoint_every_n_tokens))
+
+
+def chunk_fwd_checkpoints(q, k, v, g, beta, checkpoint_every_n_tokens: int, scale=None,
+                          initial_state=None, cu_seqlens=None, output_final_state=False,
+                          path: str = "auto", stream=None):
+    """``chunk_fwd`` on device tensors that also returns state checkpoints
+    (libgdr ``gdr_chunk_fwd_ckpt``).
+
+    Returns (o, ht or None, state_checkpoints [bound, H, dk, dv] f32,
+    checkpoint_cu_starts [N + 1] int32): checkpoint m (1-based) of segment n is the
+    state after the segment's first m * checkpoint_every_n_tokens tokens, in row
+    checkpoint_cu_starts[n] + m - 1; rows past checkpoint_cu_starts[N] are not written.
+    """
+    dev = q.device
+    T, H, dk, dv = q.shape[0], v.shape[1], q.shape[-1], v.shape[2]
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    n_seq = cu_seqlens.numel() - 1
+    scale = dk ** -0.5 if scale is None else scale
+    o = torch.empty(T, H, dv, dtype=torch.bfloat16, device=dev)
+    ht = (torch.empty(n_seq, H, dk, dv, dtype=torch.float32, device=dev)
+          if output_final_state else None)
+    rows = checkpoint_count_bound(T, checkpoint_every_n_tokens)
+    ck = torch.empty(max(rows, 1), H, dk, dv, dtype=torch.float32, device=dev)
+    starts = torch.empty(n_seq + 1, dtype=torch.int32, device=dev)
+    ws = _workspace(workspace_bytes(T, n_seq, H, dk, dv, path), dev)
+    ds = [_Desc(t) for t in (q, k, v, g, beta)]
+    dh0, do, dht = _d(initial_state), _Desc(o), _d(ht)
+    dck = _Desc(ck[:rows] if rows > 0 else ck[:0])
+    rc = nat.lib().gdr_chunk_fwd_ckpt(
+        ds[0].ref, ds[1].ref, ds[2].ref, ds[3].ref, ds[4].ref, ctypes.c_float(scale),
+        _ref(dh0), _ptr(cu_seqlens), n_seq, do.ref, _ref(dht), dck.ref, _ptr(starts),
+        int(checkpoint_every_n_tokens), nat.PATHS[path], ctypes.c_void_p(ws.data_ptr()),
+        ws.numel(), _stream(stream))
+    nat.check(rc, "gdr_chunk_fwd_ckpt")
+    return o, ht, ck[:rows], starts
+
+
 def chunk_fwd_alloc(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
                     output_final_state=False, stream=None):
     """Same as ``chunk_fwd`` on device tensors, but through ``gdr_chunk_fwd``,

@@ -74,6 +74,7 @@ struct Problem {
   int32_t n_seq, Hk, H, D;
   Desc q, k, v, g, beta, o, h0, ht;
   bool has_h0, has_ht;
+  Ckpt ck{};  // state checkpoints (ck.h null: none)
 };
 
 int validate_fwd(const gdr_tensor_t *q, const gdr_tensor_t *k, const gdr_tensor_t *v,
@@ -176,6 +177,7 @@ FusedArgs fused_args(const Problem &P, float scale, void *work) {
   a.h0 = P.has_h0 ? reinterpret_cast<const float *>(P.h0.p) : nullptr;
   a.o = P.o.p; a.o_st = P.o.stride[0]; a.o_sh = P.o.stride[1];
   a.ht = P.has_ht ? reinterpret_cast<float *>(P.ht.p) : nullptr;
+  a.ckpt = P.ck;
   a.workspace = work;
   return a;
 }
@@ -192,6 +194,9 @@ int run_fwd(const Problem &P, float scale, const int32_t *cu, int32_t path, void
     a.seg = ix.seg;
     e = launch_chunk_index(cu, P.n_seq, P.T, ix.seg, nullptr, 0, ix.n_chunks, stream);
     if (e != cudaSuccess) return GDR_ERR_CUDA;
+    if (P.ck.h && (e = launch_ckpt_offsets(ix.seg, P.n_seq, P.ck.every,
+                                           const_cast<int32_t *>(P.ck.off), stream)) != cudaSuccess)
+      return GDR_ERR_CUDA;
     e = launch_fused(a, stream);
     return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
   }
@@ -213,12 +218,15 @@ int run_fwd(const Problem &P, float scale, const int32_t *cu, int32_t path, void
   const StageShapes s{P.T, P.n_seq, P.Hk, P.H, P.D, cap};
   e = launch_chunk_index(cu, P.n_seq, P.T, ix.seg, ix.chunks, cap, ix.n_chunks, stream);
   if (e != cudaSuccess) return GDR_ERR_CUDA;
+  if (P.ck.h && (e = launch_ckpt_offsets(ix.seg, P.n_seq, P.ck.every,
+                                         const_cast<int32_t *>(P.ck.off), stream)) != cudaSuccess)
+    return GDR_ERR_CUDA;
   e = launch_prep(s, view_of(P.k), view_of(P.v), view_of(P.g), view_of(P.beta), vw, vu, vg,
                   ix.seg, ix.chunks, ix.n_chunks, stream);
   if (e != cudaSuccess) return GDR_ERR_CUDA;
   e = launch_scan(s, view_of(P.k), vw, vu, vg,
                   P.has_h0 ? reinterpret_cast<const float *>(P.h0.p) : nullptr, h, vv,
-                  P.has_ht ? reinterpret_cast<float *>(P.ht.p) : nullptr, ix.seg, stream);
+                  P.has_ht ? reinterpret_cast<float *>(P.ht.p) : nullptr, P.ck, ix.seg, stream);
   if (e != cudaSuccess) return GDR_ERR_CUDA;
   e = launch_out(s, view_of(P.q), view_of(P.k), vv, h, vg, scale, view_of(P.o), ix.seg,
                  ix.chunks, ix.n_chunks, stream);
@@ -265,6 +273,8 @@ const char *gdr_status_string(int status) {
     case GDR_ERR_DEVICE: return "the current device is not sm_103 (GB300)";
     case GDR_ERR_SCRATCH_LIMIT:
       return "problem too large for the 4 MiB static scratch of gdr_chunk_out_noalloc";
+    case GDR_ERR_CKPT:
+      return "checkpoint interval not a positive multiple of 64, or checkpoint buffers wrong";
     default: return "unknown status";
   }
 }
@@ -298,6 +308,46 @@ int gdr_chunk_fwd_ws(const gdr_tensor_t *q, const gdr_tensor_t *k, const gdr_ten
   const int chosen = choose_path(P, scale, path);
   if (chosen < 0) return chosen;
   if (P.n_seq == 0) return GDR_OK;
+  const size_t need = ws_bytes_for(P.T, P.n_seq, P.H, P.D, chosen);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return GDR_ERR_WORKSPACE;
+  return run_fwd(P, scale, cu_seqlens, chosen, workspace, workspace_bytes, stream);
+}
+
+int64_t gdr_ckpt_count_bound(int64_t T, int32_t ckpt_every) {
+  if (T < 0 || ckpt_every <= 0) return 0;
+  return T / ckpt_every;
+}
+
+int gdr_chunk_fwd_ckpt(const gdr_tensor_t *q, const gdr_tensor_t *k, const gdr_tensor_t *v,
+                       const gdr_tensor_t *g, const gdr_tensor_t *beta, float scale,
+                       const gdr_tensor_t *h0, const int32_t *cu_seqlens, int32_t n_seq,
+                       gdr_tensor_t *o, gdr_tensor_t *ht, gdr_tensor_t *state_checkpoints,
+                       int32_t *checkpoint_cu_starts, int32_t checkpoint_every_n_tokens,
+                       int32_t path, void *workspace, size_t workspace_bytes,
+                       cudaStream_t stream) {
+  Problem P;
+  int r = validate_fwd(q, k, v, g, beta, h0, cu_seqlens, n_seq, o, ht, &P);
+  if (r) return r;
+  const int32_t every = checkpoint_every_n_tokens;
+  if (every <= 0 || every % kChunk != 0) return GDR_ERR_CKPT;
+  if (!state_checkpoints || !checkpoint_cu_starts) return GDR_ERR_NULL;
+  Desc C;
+  if ((r = read_desc(state_checkpoints, GDR_F32, 4, &C))) return r;
+  if (C.shape[0] < P.T / every || C.shape[1] != P.H || C.shape[2] != P.D || C.shape[3] != P.D)
+    return GDR_ERR_CKPT;
+  if (!compact(C)) return GDR_ERR_STRIDE;
+  P.ck.h = reinterpret_cast<float *>(C.p);
+  P.ck.off = checkpoint_cu_starts;
+  P.ck.every = every;
+  if ((r = device_ok())) return r;
+  const int chosen = choose_path(P, scale, path);
+  if (chosen < 0) return chosen;
+  if (P.n_seq == 0) {
+    return cudaMemsetAsync(checkpoint_cu_starts, 0, sizeof(int32_t), stream) == cudaSuccess
+               ? GDR_OK
+               : GDR_ERR_CUDA;
+  }
   const size_t need = ws_bytes_for(P.T, P.n_seq, P.H, P.D, chosen);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
     return GDR_ERR_WORKSPACE;
@@ -435,7 +485,7 @@ int gdr_state_scan(const gdr_tensor_t *k, const gdr_tensor_t *w, const gdr_tenso
   if (e == cudaSuccess)
     e = launch_scan(s, view_of(K), view_of(Wd), view_of(Ud), view_of(Gc),
                     h0 ? reinterpret_cast<const float *>(H0.p) : nullptr, Hd.p, view_of(Vn),
-                    ht ? reinterpret_cast<float *>(HT.p) : nullptr, ix.seg, stream);
+                    ht ? reinterpret_cast<float *>(HT.p) : nullptr, Ckpt{}, ix.seg, stream);
   return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 

@@ -96,7 +96,7 @@ struct ChunkVec {
   float eL;                    // exp(G_last)
   float Gref;                  // max_j G_j
   int32_t fac;                 // 1: max G - min G is small enough to factor 2^(G_i - G_j)
-  float pad;
+  int32_t ckrow;               // checkpoint row of the state entering this chunk, or -1
 };
 // 2^(G_i - G_j) = 2^(G_i - Gref) 2^(Gref - G_j) with both factors normal fp32 numbers
 // as long as the chunk's range of G (log2 units) stays below this bound.
@@ -126,6 +126,7 @@ struct Params {
   __nv_bfloat16 *o;
   int64_t o_st, o_sh;
   float *ht;
+  Ckpt ckpt;                // state checkpoints (ckpt.h null: none)
   const SegInfo *seg;
   const int32_t *order;     // non-empty segments, longest first
   const int32_t *n_active;  // number of non-empty segments
@@ -220,6 +221,7 @@ __device__ void fetch_unit(const Params &p, Small *sm, int slot) {
 }
 
 // ------------------------------------------------------------------ roles
+template <bool kCkpt>
 __device__ void role_producer(const Params &p, Small *sm, uint8_t *base,
                               const CUtensorMap *mq, const CUtensorMap *mk,
                               const CUtensorMap *mv) {
@@ -312,6 +314,10 @@ __device__ void role_producer(const Params &p, Small *sm, uint8_t *base,
           cv.eL = ex2(GL);
           cv.Gref = gmax;
           cv.fac = fac ? 1 : 0;
+          if constexpr (kCkpt)
+            cv.ckrow = (c > 0 && (c * kChunk) % p.ckpt.every == 0)
+                           ? p.ckpt.off[ui.seq] + (c * kChunk) / p.ckpt.every - 1
+                           : -1;
         }
       }
       __syncwarp();
@@ -762,9 +768,28 @@ __device__ __noinline__ void state_from_h0(const Params &p, uint32_t taddr, int6
   tmem_st_wait();
 }
 
-// The state warpgroup.  `row` is this thread's TMEM lane = value dimension dv.
+// Row dv of S^T (TMEM, fp32) -> column dv of a [dk][dv] fp32 state at `dst` (state
+// checkpoints), kept out of line.
+__device__ __noinline__ void store_state(uint32_t taddr, float *dst, int D, int dv) {
+#pragma unroll 1
+  for (int cb = 0; cb < 4; ++cb) {
+    uint32_t r[32];
+    tmem_ld32(taddr + cb * 32, r);
+    tmem_ld_wait();
+    if (dv < D) {
+#pragma unroll
+      for (int u = 0; u < 32; ++u)
+        if (cb * 32 + u < D) dst[(int64_t)(cb * 32 + u) * D + dv] = __uint_as_float(r[u]);
+    }
+  }
+}
+
+// The state warpgroup.  `row` is this thread's TMEM lane = value dimension dv.  With
+// kCkpt it also writes the state checkpoints (a separate instantiation, so that the
+// plain forward's code is untouched).
 // Per chunk: S^T -> bf16 (A operand of Y and O1) and e^{G_last} S^T; Y -> bf16;
 // V'^T -> bf16 V'^T and V''^T; and the previous chunk's output.
+template <bool kCkpt>
 __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
   const uint32_t tb = sm->tmem_base;
   const uint32_t lane_base = (uint32_t)(row & ~31);
@@ -839,6 +864,13 @@ __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
       if (g >= 1 && !wait_wg(sm, sm->o1_full, (g - 1) & 1, 0x408, kBarState)) { ok = false; break; }
       tc_fence_after();
       if (c == 0) state_from_h0(p, tmem_addr(tb + TM_S, lane_base, 0), sidx, dv);
+      if constexpr (kCkpt) {
+        // the state entering this chunk, after c * 64 of the segment's tokens (row chosen
+        // by the producer)
+        if (cv.ckrow >= 0)
+          store_state(tmem_addr(tb + TM_S, lane_base, 0),
+                      p.ckpt.h + ((int64_t)cv.ckrow * p.H + ui.head) * D * D, D, dv);
+      }
       // S^T -> bf16 pairs (A operand of Y and O1), and e^{G_last} S^T (the base of this
       // chunk's S^T += V''^T K) back in place
       const float eL = cv.eL;
@@ -932,11 +964,22 @@ __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
         }
       }
     }
+    if constexpr (kCkpt) {
+      const int seg_len = ui.end - ui.t0;
+      if (seg_len % p.ckpt.every == 0) {
+        const int64_t r = p.ckpt.off[ui.seq] + seg_len / p.ckpt.every - 1;
+        store_state(tmem_addr(tb + TM_S, lane_base, 0), p.ckpt.h + (r * p.H + ui.head) * D * D,
+                    D, dv);
+      }
+    }
     if (!epi_read(g - 1)) break;
     epi_store();
   }
 }
 
+// kCkpt: the variant that also writes state checkpoints (a separate kernel, so the plain
+// forward's code is not touched by it)
+template <bool kCkpt>
 __global__ void __launch_bounds__(kThreads, 1)
     k_fused(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
             const __grid_constant__ CUtensorMap mv, const Params p) {
@@ -995,7 +1038,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
 
   if (warp == 0) {
-    role_producer(p, sm, base, &mq, &mk, &mv);
+    role_producer<kCkpt>(p, sm, base, &mq, &mk, &mv);
   } else if (warp == 1) {
     if (lane == 0) role_issue_p(p, sm, base);
   } else if (warp == 2) {
@@ -1003,7 +1046,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < 7) {
     role_prep(p, sm, base, 32 * (warp & 3) + lane);
   } else {
-    role_state(p, sm, base, 32 * (warp & 3) + lane);
+    role_state<kCkpt>(p, sm, base, 32 * (warp & 3) + lane);
   }
   tc_fence_before();
   __syncthreads();
@@ -1154,7 +1197,9 @@ cudaError_t launch_fused(const FusedArgs &a, cudaStream_t stream) {
     int n = 0;
     if ((e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return e;
-    if ((e = cudaFuncSetAttribute(k_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(k_fused<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)kSmemBytes)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(k_fused<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)kSmemBytes)) != cudaSuccess)
       return e;
     g_num_sms[dev] = n;
@@ -1178,6 +1223,7 @@ cudaError_t launch_fused(const FusedArgs &a, cudaStream_t stream) {
   p.o_st = a.o_st;
   p.o_sh = a.o_sh;
   p.ht = a.ht;
+  p.ckpt = a.ckpt;
   p.seg = a.seg;
   p.order = order;
   p.n_active = counters + 1;
@@ -1189,7 +1235,10 @@ cudaError_t launch_fused(const FusedArgs &a, cudaStream_t stream) {
   int grid = g_num_sms[dev];
   if (units_max < grid) grid = (int)units_max;
   if (grid <= 0) return cudaSuccess;
-  k_fused<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+  if (p.ckpt.h)
+    k_fused<true><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+  else
+    k_fused<false><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 

@@ -110,6 +110,26 @@ __global__ void k_chunk_table(const SegInfo *__restrict__ seg, int32_t n_seq,
   }
 }
 
+// Checkpoint offsets: exclusive prefix of floor(len / every) over the segments.
+__global__ void __launch_bounds__(kScanThreads)
+    k_ckpt_offsets(const SegInfo *__restrict__ seg, int32_t n_seq, int32_t every,
+                   int32_t *off) {
+  __shared__ int warp_buf[32];
+  __shared__ int carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < n_seq; base += kScanThreads) {
+    const int i = base + (int)threadIdx.x;
+    const int nc = i < n_seq ? (seg[i].end - seg[i].start) / every : 0;
+    const int incl = block_inclusive_scan<false>(nc, warp_buf);
+    if (i < n_seq) off[i] = carry + incl - nc;
+    __syncthreads();
+    if (threadIdx.x == kScanThreads - 1) carry += incl;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) off[n_seq] = carry;
+}
+
 __global__ void k_check_cu(const int32_t *__restrict__ cu, int32_t n_seq, int64_t T,
                            int32_t *out2) {
   // out2[0]: count of bad offsets, out2[1]: first bad index (or -1); single block
@@ -126,6 +146,13 @@ __global__ void k_check_cu(const int32_t *__restrict__ cu, int32_t n_seq, int64_
 }
 
 }  // namespace
+
+cudaError_t launch_ckpt_offsets(const SegInfo *seg, int32_t n_seq, int32_t every, int32_t *off,
+                                cudaStream_t stream) {
+  if (every <= 0) return cudaErrorInvalidValue;
+  k_ckpt_offsets<<<1, kScanThreads, 0, stream>>>(seg, n_seq, every, off);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_chunk_index(const int32_t *cu, int32_t n_seq, int64_t T, SegInfo *seg,
                                ChunkInfo *chunks, int64_t chunk_cap, int32_t *n_chunks,

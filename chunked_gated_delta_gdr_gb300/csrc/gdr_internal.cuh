@@ -67,9 +67,19 @@ struct StageShapes {
 cudaError_t launch_prep(const StageShapes &s, View k, View v, View g, View beta, View w,
                         View u, View gcum, const SegInfo *seg, const ChunkInfo *chunks,
                         const int32_t *n_chunks, cudaStream_t stream);
+// State checkpoints: state after every `every` tokens of each segment (every a positive
+// multiple of 64; 0 = none), rows off[n] .. off[n+1]-1 of h [rows, H, D, D] for segment n.
+struct Ckpt {
+  float *h;
+  const int32_t *off;
+  int32_t every;
+};
 cudaError_t launch_scan(const StageShapes &s, View k, View w, View u, View gcum,
-                        const float *h0, void *h, View v_new, float *ht, const SegInfo *seg,
-                        cudaStream_t stream);
+                        const float *h0, void *h, View v_new, float *ht, Ckpt ck,
+                        const SegInfo *seg, cudaStream_t stream);
+// off[n] = sum over segments before n of floor(len / every); off[n_seq] = total
+cudaError_t launch_ckpt_offsets(const SegInfo *seg, int32_t n_seq, int32_t every, int32_t *off,
+                                cudaStream_t stream);
 cudaError_t launch_out(const StageShapes &s, View q, View k, View v_new, const void *h,
                        View gcum, float scale, View o, const SegInfo *seg,
                        const ChunkInfo *chunks, const int32_t *n_chunks, cudaStream_t stream);
@@ -89,6 +99,7 @@ struct FusedArgs {
   void *o;
   int64_t o_st, o_sh;
   float *ht;
+  Ckpt ckpt;
   const SegInfo *seg;
   void *workspace;  // fused-path scratch (work list etc.)
 };

@@ -116,7 +116,8 @@ struct ScanSmem {
 template <int D>
 __global__ void __launch_bounds__(128)
     k_scan(int32_t H, int32_t group, View k, View w, View u, View gcum, const float *h0,
-           __nv_bfloat16 *hbuf, View v_new, float *ht, const SegInfo *__restrict__ seg) {
+           __nv_bfloat16 *hbuf, View v_new, float *ht, Ckpt ck,
+           const SegInfo *__restrict__ seg) {
   extern __shared__ float sm[];
   constexpr int L = ScanSmem<D>::kLd;
   const int n = blockIdx.x, h = blockIdx.y, jb = blockIdx.z * kScanCols, tid = threadIdx.x;
@@ -130,11 +131,22 @@ __global__ void __launch_bounds__(128)
     const int d = idx / kScanCols, j = idx % kScanCols;
     S[d * 33 + j] = h0 ? h0[sbase + (int64_t)d * D + jb + j] : 0.f;
   }
+  // state of this block's columns -> checkpoint row `row` (the state after the
+  // segment's first (row - first row + 1) * every tokens)
+  auto store_ckpt = [&](int64_t row) {
+    float *dst = ck.h + (row * H + h) * D * D;
+    for (int idx = tid; idx < D * kScanCols; idx += blockDim.x) {
+      const int d = idx / kScanCols, j = idx % kScanCols;
+      dst[(int64_t)d * D + jb + j] = S[d * 33 + j];
+    }
+  };
   for (int c = 0; c < si.n_chunks; ++c) {
     const int64_t cid = si.chunk_off + c;
     const int64_t t0 = si.start + (int64_t)c * kChunk;
     const int len = min(kChunk, si.end - (int)t0);
     __syncthreads();
+    if (ck.h && c > 0 && (c * kChunk) % ck.every == 0)
+      store_ckpt(ck.off[n] + (c * kChunk) / ck.every - 1);
     __nv_bfloat16 *hc = hbuf + (cid * H + h) * D * D;
     for (int idx = tid; idx < D * kScanCols; idx += blockDim.x) {
       const int d = idx / kScanCols, j = idx % kScanCols;
@@ -180,13 +192,15 @@ __global__ void __launch_bounds__(128)
       S[d * 33 + j] = acc;
     }
   }
+  if (ht || ck.h) __syncthreads();
   if (ht) {
-    __syncthreads();
     for (int idx = tid; idx < D * kScanCols; idx += blockDim.x) {
       const int d = idx / kScanCols, j = idx % kScanCols;
       ht[sbase + (int64_t)d * D + jb + j] = S[d * 33 + j];
     }
   }
+  const int seg_len = si.end - si.start;
+  if (ck.h && seg_len > 0 && seg_len % ck.every == 0) store_ckpt(ck.off[n] + seg_len / ck.every - 1);
 }
 
 // ---------------------------------------------------------------- stage 3
@@ -285,8 +299,8 @@ cudaError_t launch_prep(const StageShapes &s, View k, View v, View g, View beta,
 }
 
 cudaError_t launch_scan(const StageShapes &s, View k, View w, View u, View gcum,
-                        const float *h0, void *h, View v_new, float *ht, const SegInfo *seg,
-                        cudaStream_t stream) {
+                        const float *h0, void *h, View v_new, float *ht, Ckpt ck,
+                        const SegInfo *seg, cudaStream_t stream) {
   if (s.n_seq <= 0 || s.H <= 0) return cudaSuccess;
   dim3 grid((unsigned)s.n_seq, (unsigned)s.H, (unsigned)(s.D / kScanCols));
   auto *hb = reinterpret_cast<__nv_bfloat16 *>(h);
@@ -294,11 +308,11 @@ cudaError_t launch_scan(const StageShapes &s, View k, View w, View u, View gcum,
   if (s.D == 64) {
     if ((e = set_smem(k_scan<64>, ScanSmem<64>::bytes)) != cudaSuccess) return e;
     k_scan<64><<<grid, 128, ScanSmem<64>::bytes, stream>>>(s.H, s.H / s.Hk, k, w, u, gcum, h0,
-                                                           hb, v_new, ht, seg);
+                                                           hb, v_new, ht, ck, seg);
   } else {
     if ((e = set_smem(k_scan<128>, ScanSmem<128>::bytes)) != cudaSuccess) return e;
     k_scan<128><<<grid, 128, ScanSmem<128>::bytes, stream>>>(s.H, s.H / s.Hk, k, w, u, gcum,
-                                                             h0, hb, v_new, ht, seg);
+                                                             h0, hb, v_new, ht, ck, seg);
   }
   return cudaGetLastError();
 }

@@ -69,7 +69,9 @@ enum gdr_status {
   GDR_ERR_CUDA = -10,     /* a CUDA runtime call or kernel launch failed         */
   GDR_ERR_ALIGN = -11,    /* a base pointer or row stride is not 16-byte aligned */
   GDR_ERR_DEVICE = -12,   /* the current device is not sm_103 (GB300)            */
-  GDR_ERR_SCRATCH_LIMIT = -13 /* problem too large for gdr_chunk_out_noalloc's static scratch */
+  GDR_ERR_SCRATCH_LIMIT = -13, /* problem too large for gdr_chunk_out_noalloc's static scratch */
+  GDR_ERR_CKPT = -14           /* checkpoint interval not a positive multiple of 64, or
+                                  checkpoint buffer of the wrong type, shape or size  */
 };
 
 /* Execution paths of the forward. */
@@ -124,6 +126,36 @@ int gdr_chunk_fwd_ws(const gdr_tensor_t *q, const gdr_tensor_t *k, const gdr_ten
                      const gdr_tensor_t *h0, const int32_t *cu_seqlens, int32_t n_seq,
                      gdr_tensor_t *o, gdr_tensor_t *ht, int32_t path, void *workspace,
                      size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * gdr_chunk_fwd_ckpt -- gdr_chunk_fwd_ws that also writes state checkpoints every
+ * checkpoint_every_n_tokens tokens of each segment, for prefix caching.  The FlashInfer
+ * KDA prefill keeps this surface (state_checkpoints / checkpoint_cu_starts /
+ * checkpoint_every_n_tokens kwargs, "feat(cake_kda): add paired recurrent training for
+ * SM100a and SM103a", the released inference surface kept by the cherry-picked commit);
+ * the pages describe no layout, so the one below is this library's.
+ *   checkpoint_every_n_tokens  positive multiple of 64 (the chunk size).
+ *   state_checkpoints   [rows, H, dk, dv] fp32 out, compact; rows >=
+ *                       gdr_ckpt_count_bound(T, checkpoint_every_n_tokens).  Checkpoint m
+ *                       (m = 1 .. floor(len_n / every)) of segment n is the state S
+ *                       ([dk][dv], as ht) after the segment's first m * every tokens, in row
+ *                       checkpoint_cu_starts[n] + m - 1.  Other rows are not written.
+ *   checkpoint_cu_starts  device int32 [n_seq + 1] out: the running sum of
+ *                       floor(len_n / every) (lengths after the cu_seqlens reading); the last
+ *                       entry is the number of checkpoints written.
+ * Workspace as gdr_chunk_fwd_ws.  Errors: as gdr_chunk_fwd_ws, plus GDR_ERR_CKPT.
+ */
+int gdr_chunk_fwd_ckpt(const gdr_tensor_t *q, const gdr_tensor_t *k, const gdr_tensor_t *v,
+                       const gdr_tensor_t *g, const gdr_tensor_t *beta, float scale,
+                       const gdr_tensor_t *h0, const int32_t *cu_seqlens, int32_t n_seq,
+                       gdr_tensor_t *o, gdr_tensor_t *ht, gdr_tensor_t *state_checkpoints,
+                       int32_t *checkpoint_cu_starts, int32_t checkpoint_every_n_tokens,
+                       int32_t path, void *workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
+
+/* Rows gdr_chunk_fwd_ckpt may write: floor(T / checkpoint_every_n_tokens) (0 for bad
+ * arguments). */
+int64_t gdr_ckpt_count_bound(int64_t T, int32_t checkpoint_every_n_tokens);
 
 /* Upper bound on the number of 64-token chunks: ceil(T / 64) + n_seq. */
 int64_t gdr_chunk_count_bound(int64_t T, int32_t n_seq);

@@ -182,3 +182,38 @@ def test_binding_raises_without_gpu(lib):
     q = torch.zeros(64, 1, 64, dtype=torch.bfloat16)
     with pytest.raises(Exception):
         api.chunk_fwd(q, q, q, torch.zeros(64, 1), torch.zeros(64, 1, dtype=torch.bfloat16))
+
+
+def _call_ckpt(lib, a, ck, starts, every, path=0, ws=0x40000, ws_bytes=1 << 40):
+    r = lambda d: None if d is None else ctypes.byref(d)
+    return lib.gdr_chunk_fwd_ckpt(r(a["q"]), r(a["k"]), r(a["v"]), r(a["g"]), r(a["beta"]),
+                                  ctypes.c_float(0.125), r(a["h0"]), a["cu"], a["n_seq"],
+                                  r(a["o"]), r(a["ht"]), r(ck), starts, every, path,
+                                  ctypes.c_void_p(ws), ws_bytes, None)
+
+
+@pytest.mark.parametrize("case,code", [
+    ("every_zero", -14), ("every_not_64", -14), ("rows_short", -14), ("ckpt_dtype", -2),
+    ("ckpt_heads", -14), ("starts_null", -1), ("ckpt_null", -1), ("ckpt_noncompact", -4),
+])
+def test_checkpoint_validation_errors(lib, case, code):
+    f = _Fake()
+    T, H, D = f.T, f.H, f.D
+    every = {"every_zero": 0, "every_not_64": 96}.get(case, 64)
+    rows = T // 64
+    ck = {
+        "rows_short": f.t([rows - 1, H, D, D], nat.GDR_F32),
+        "ckpt_dtype": f.t([rows, H, D, D], nat.GDR_BF16),
+        "ckpt_heads": f.t([rows, H + 1, D, D], nat.GDR_F32),
+        "ckpt_null": None,
+        "ckpt_noncompact": f.t([rows, H, D, D], nat.GDR_F32, strides=[2 * H * D * D, D * D, D, 1]),
+    }.get(case, f.t([rows, H, D, D], nat.GDR_F32))
+    starts = None if case == "starts_null" else ctypes.c_void_p(0x30000)
+    rc = _call_ckpt(lib, f.args(), ck, starts, every)
+    assert rc == code, (case, rc)
+
+
+def test_checkpoint_count_bound(lib):
+    assert lib.gdr_ckpt_count_bound(1000, 64) == 15
+    assert lib.gdr_ckpt_count_bound(1000, 0) == 0
+    assert lib.gdr_ckpt_count_bound(-1, 64) == 0
