@@ -286,10 +286,25 @@ def pin_checkpoint_resume(rec):
         np.testing.assert_allclose(h2[0], ht[0], rtol=0, atol=1e-12)
 
 
+def pin_affine_state_carry(rec):
+    # the state after a span of tokens is affine in the state before it:
+    # S_out = M S_in + R with M the span's transition (run from S_in = I with v = 0) and R
+    # its zero-start state (run from S_in = 0); the intra-sequence split chains pieces
+    # this way (the CP final_correction of "feat(cake_kda): add paired recurrent training
+    # for SM100a and SM103a" carries the state across ranks the same way)
+    d = _random_f64(121, [77], 1, 2, 5, 5)
+    _, ht = _run(rec, d)
+    eye = np.broadcast_to(np.eye(5), (1, 2, 5, 5)).copy()
+    _, M = _run(rec, dict(d, v=np.zeros_like(d["v"]), h0=eye))
+    _, R = _run(rec, dict(d, h0=np.zeros_like(d["h0"])))
+    np.testing.assert_allclose(ht[0], np.einsum("hij,hjk->hik", M[0], d["h0"][0]) + R[0],
+                               rtol=0, atol=1e-12)
+
+
 PINS = [pin_hand_worked, pin_chunked_form, pin_unrolled_products, pin_beta_zero,
         pin_overwrite, pin_single_token, pin_ghosts, pin_chaining, pin_grouped_heads,
         pin_linearity, pin_segment_reading, pin_bf16_decoding, pin_checkpoint_prefixes,
-        pin_checkpoint_resume]
+        pin_checkpoint_resume, pin_affine_state_carry]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
