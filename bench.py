@@ -36,7 +36,7 @@ def parse():
     p.add_argument("--steps", type=int, default=100)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--path", choices=["auto", "fused", "staged"], default="auto")
+    p.add_argument("--path", choices=["auto", "fused", "staged", "fused_whole"], default="auto")
     p.add_argument("--workload", default=WORKLOAD)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -297,9 +297,16 @@ def bench_ours(args):
     total_ms = max_over_ranks(sum(per), dist, dev)
     ms_per_step = total_ms / args.steps
     value = job_tokens_per_s(ws, T, args.steps, total_ms)
-    fused = path in ("auto", "fused") and _fused_available(api, wd, w)
-    # fused: chunk enumeration, work list, [empty-segment states], fused kernel
-    launches_per_step = (3 + bool(w.want_ht)) if fused else 4
+    fused = path in ("auto", "fused", "fused_whole") and _fused_available(api, wd, w)
+    pieces = api.split_pieces(T, N, H) if path in ("auto", "fused") else 1
+    if fused and pieces > 1:
+        # chunk enumeration, split units, [empty-segment states], pass A, combine, pass B
+        launches_per_step = 5 + bool(w.want_ht)
+    elif fused:
+        # chunk enumeration, work list, [empty-segment states], fused kernel
+        launches_per_step = 3 + bool(w.want_ht)
+    else:
+        launches_per_step = 4
     hbm, tflops, peak_kind = peaks()
     alg_b = algorithmic_bytes(w)
     alg_f = algorithmic_flops(w)
@@ -311,7 +318,7 @@ def bench_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if fused else "f32", "data": "synthetic",
             "config": {"workload": w.name, "T": T, "H": H, "Hk": w.Hk, "d": D, "n_seq": N,
-                       "n_chunks": w.n_chunks(), "path": path,
+                       "n_chunks": w.n_chunks(), "path": path, "split_pieces": pieces if fused else 1,
                        "l2": (f"inputs ({alg_b / 1e9:.2f} GB) exceed the 129 MB L2; "
                               "no flush between steps"),
                        "per_rank": "each rank runs its own copy of the workload"},

@@ -16,6 +16,7 @@ from .api import (  # noqa: F401
     chunk_prep,
     clear_device_status,
     device_status,
+    split_pieces,
     stage_workspace_bytes,
     state_scan,
     wait_selftest,

@@ -9,7 +9,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libgdr.so")
 
 GDR_BF16, GDR_F32, GDR_I32 = 1, 2, 3
-PATHS = {"auto": 0, "fused": 1, "staged": 2}
+PATHS = {"auto": 0, "fused": 1, "staged": 2, "fused_whole": 3}
 
 STATUS = {
     0: "GDR_OK", -1: "GDR_ERR_NULL", -2: "GDR_ERR_DTYPE", -3: "GDR_ERR_SHAPE",
@@ -38,6 +38,7 @@ SIGNATURES = {
     "gdr_chunk_fwd_ckpt": (ctypes.c_int, [_T, _T, _T, _T, _T, _f32, _T, _vp, _i32, _T, _T, _T,
                                           _vp, _i32, _i32, _vp, _sz, _vp]),
     "gdr_ckpt_count_bound": (_i64, [_i64, _i32]),
+    "gdr_fused_split_pieces": (_i32, [_i64, _i32, _i32]),
     "gdr_chunk_count_bound": (_i64, [_i64, _i32]),
     "gdr_stage_workspace_bytes": (_sz, [_i64, _i32]),
     "gdr_chunk_index": (ctypes.c_int, [_vp, _i32, _i64, _vp, _vp, _vp, _vp]),

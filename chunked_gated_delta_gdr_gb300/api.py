@@ -127,6 +127,12 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor
     return o, ht
 
 
+def split_pieces(T: int, n_seq: int, H: int) -> int:
+    """Pieces per long segment of the fused path's sequence split on the current device
+    (1: the fused path runs every (segment, head) whole)."""
+    return int(nat.lib().gdr_fused_split_pieces(T, n_seq, H))
+
+
 def checkpoint_count_bound(T: int, checkpoint_every_n_tokens: int) -> int:
     """Rows ``chunk_fwd_checkpoints`` may write: floor(T / checkpoint_every_n_tokens)."""
     return int(nat.lib().gdr_ckpt_count_bound(T, checkpoint_every_n_tokens))

@@ -182,6 +182,30 @@ FusedArgs fused_args(const Problem &P, float scale, void *work) {
   return a;
 }
 
+// Pieces per segment of the fused path's sequence split on the current device (1: none).
+int split_plan(int64_t T, int32_t n_seq, int32_t H, bool ckpt, int *lead = nullptr) {
+  static int sms[64] = {0};
+  int lead_dummy = 1;
+  if (!lead) lead = &lead_dummy;
+  *lead = 1;
+  // no segment can be cut when none reaches three of the shortest pieces
+  if (ckpt || n_seq <= 0 || T <= (int64_t)(3 * kSplitMinChunks - 1) * kChunk) return 1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 1;
+  }
+  if (sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return 1;
+    }
+    sms[dev] = n;
+  }
+  return split_pieces((int64_t)n_seq * H, sms[dev], lead);
+}
+
 int run_fwd(const Problem &P, float scale, const int32_t *cu, int32_t path, void *ws,
             size_t ws_bytes, cudaStream_t stream) {
   if (P.n_seq == 0) return GDR_OK;
@@ -189,7 +213,7 @@ int run_fwd(const Problem &P, float scale, const int32_t *cu, int32_t path, void
   char *rest = reinterpret_cast<char *>(ws) + ix.bytes;
   const int64_t cap = chunk_bound(P.T, P.n_seq);
   cudaError_t e;
-  if (path == GDR_PATH_FUSED) {
+  if (path == GDR_PATH_FUSED || path == GDR_PATH_FUSED_WHOLE) {
     FusedArgs a = fused_args(P, scale, rest);
     a.seg = ix.seg;
     e = launch_chunk_index(cu, P.n_seq, P.T, ix.seg, nullptr, 0, ix.n_chunks, stream);
@@ -197,6 +221,24 @@ int run_fwd(const Problem &P, float scale, const int32_t *cu, int32_t path, void
     if (P.ck.h && (e = launch_ckpt_offsets(ix.seg, P.n_seq, P.ck.every,
                                            const_cast<int32_t *>(P.ck.off), stream)) != cudaSuccess)
       return GDR_ERR_CUDA;
+    int lead = 1;
+    const int pieces =
+        path == GDR_PATH_FUSED ? split_plan(P.T, P.n_seq, P.H, P.ck.h != nullptr, &lead) : 1;
+    if (pieces <= 1) {
+      e = launch_fused(a, stream);
+      return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+    }
+    // sequence split: pass A (first pieces, R and M of the middle ones), the chain of
+    // initial states, pass B (the later pieces)
+    const SplitWs sw = carve_split(rest + fused_workspace_bytes(P.T, P.n_seq, P.H), P.n_seq,
+                                   P.H, P.D, pieces);
+    if ((e = launch_split_units(ix.seg, P.n_seq, P.H, pieces, lead, sw, stream)) != cudaSuccess)
+      return GDR_ERR_CUDA;
+    a.split = SplitArgs{sw.ua, sw.na, sw.states, sw.counters, true};
+    if ((e = launch_fused(a, stream)) != cudaSuccess) return GDR_ERR_CUDA;
+    if ((e = launch_split_combine(sw, P.n_seq, P.H, P.D, stream)) != cudaSuccess)
+      return GDR_ERR_CUDA;
+    a.split = SplitArgs{sw.ub, sw.nb, sw.states, sw.counters + 1, false};
     e = launch_fused(a, stream);
     return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
   }
@@ -236,8 +278,11 @@ int run_fwd(const Problem &P, float scale, const int32_t *cu, int32_t path, void
 size_t ws_bytes_for(int64_t T, int32_t n_seq, int32_t H, int32_t D, int32_t path) {
   const size_t ix = carve_index(nullptr, T, n_seq).bytes;
   const size_t st = staged_bytes(T, n_seq, H, D);
-  const size_t fu = ix + fused_workspace_bytes(T, n_seq, H);
+  const size_t fw = ix + fused_workspace_bytes(T, n_seq, H);
+  const int pieces = split_plan(T, n_seq, H, false);
+  const size_t fu = fw + (pieces > 1 ? carve_split(nullptr, n_seq, H, D, pieces).bytes : 0);
   if (path == GDR_PATH_STAGED) return st;
+  if (path == GDR_PATH_FUSED_WHOLE) return fw;
   if (path == GDR_PATH_FUSED) return fu;
   return st > fu ? st : fu;
 }
@@ -245,7 +290,8 @@ size_t ws_bytes_for(int64_t T, int32_t n_seq, int32_t H, int32_t D, int32_t path
 int choose_path(const Problem &P, float scale, int32_t path) {
   if (path == GDR_PATH_STAGED) return GDR_PATH_STAGED;
   const bool fused_ok = fused_supported(fused_args(P, scale, nullptr));
-  if (path == GDR_PATH_FUSED) return fused_ok ? GDR_PATH_FUSED : GDR_ERR_PATH;
+  if (path == GDR_PATH_FUSED || path == GDR_PATH_FUSED_WHOLE)
+    return fused_ok ? path : GDR_ERR_PATH;
   if (path == GDR_PATH_AUTO) return fused_ok ? GDR_PATH_FUSED : GDR_PATH_STAGED;
   return GDR_ERR_PATH;
 }
@@ -312,6 +358,11 @@ int gdr_chunk_fwd_ws(const gdr_tensor_t *q, const gdr_tensor_t *k, const gdr_ten
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
     return GDR_ERR_WORKSPACE;
   return run_fwd(P, scale, cu_seqlens, chosen, workspace, workspace_bytes, stream);
+}
+
+int32_t gdr_fused_split_pieces(int64_t T, int32_t n_seq, int32_t H) {
+  if (T < 0 || n_seq <= 0 || H <= 0) return 1;
+  return split_plan(T, n_seq, H, false);
 }
 
 int64_t gdr_ckpt_count_bound(int64_t T, int32_t ckpt_every) {

@@ -79,8 +79,11 @@ constexpr uint32_t TM_O2 = 448;  // V'^T P^T (intra-chunk part of O^T), 64 colum
 constexpr uint32_t kTmemCols = 512;
 
 struct UnitInfo {
-  int32_t seq, head, t0, end, nch, pad0, pad1, pad2;
+  int32_t seq, head, t0, end, nch, mode, sin, sout;  // the last three: split units only
 };
+
+// kernel variants: the plain forward, with state checkpoints, split-segment pieces
+constexpr int kVarPlain = 0, kVarCkpt = 1, kVarSplit = 2;
 
 // Per-chunk vectors, computed by the producer warp from g and beta.  Five slots
 // (by chunk index): the producer refills chunk c's slot for chunk c+5 only after
@@ -127,6 +130,7 @@ struct Params {
   int64_t o_st, o_sh;
   float *ht;
   Ckpt ckpt;                // state checkpoints (ckpt.h null: none)
+  SplitArgs split;          // split-segment pieces (split.units null: none)
   const SegInfo *seg;
   const int32_t *order;     // non-empty segments, longest first
   const int32_t *n_active;  // number of non-empty segments
@@ -219,9 +223,20 @@ __device__ void fetch_unit(const Params &p, Small *sm, int slot) {
   sm->unit[slot] = ui;
   mbar_arrive(&sm->unit_full[slot]);
 }
+// the same from a split unit table
+__device__ void fetch_unit_split(const Params &p, Small *sm, int slot) {
+  const int32_t u = atomicAdd(p.counter, 1);
+  UnitInfo ui{-1, 0, 0, 0, 0, 0, 0, 0};
+  if (u < *p.split.n_units) {
+    const UnitDesc d = p.split.units[u];
+    ui = UnitInfo{d.seq, d.head, d.t0, d.end, d.nch, d.mode, d.sin, d.sout};
+  }
+  sm->unit[slot] = ui;
+  mbar_arrive(&sm->unit_full[slot]);
+}
 
 // ------------------------------------------------------------------ roles
-template <bool kCkpt>
+template <int kVar>
 __device__ void role_producer(const Params &p, Small *sm, uint8_t *base,
                               const CUtensorMap *mq, const CUtensorMap *mk,
                               const CUtensorMap *mv) {
@@ -236,7 +251,10 @@ __device__ void role_producer(const Params &p, Small *sm, uint8_t *base,
       ok = false;
       break;
     }
-    if (lane == 0) fetch_unit(p, sm, slot);
+    if (lane == 0) {
+      if constexpr (kVar == kVarSplit) fetch_unit_split(p, sm, slot);
+      else fetch_unit(p, sm, slot);
+    }
     __syncwarp();
     if (!wait_warp(sm, sm->unit_full[slot], (k / kUnitRing) & 1, 0x102)) {
       ok = false;
@@ -314,7 +332,7 @@ __device__ void role_producer(const Params &p, Small *sm, uint8_t *base,
           cv.eL = ex2(GL);
           cv.Gref = gmax;
           cv.fac = fac ? 1 : 0;
-          if constexpr (kCkpt)
+          if constexpr (kVar == kVarCkpt)
             cv.ckrow = (c > 0 && (c * kChunk) % p.ckpt.every == 0)
                            ? p.ckpt.off[ui.seq] + (c * kChunk) / p.ckpt.every - 1
                            : -1;
@@ -344,6 +362,7 @@ __device__ void issuer_drain(Small *sm) {
 // does not overflow inside the 227 KB window).
 __device__ __forceinline__ uint64_t dadd(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
+template <int kVar>
 __device__ void role_issue_p(const Params &p, Small *sm, uint8_t *base) {
   const uint32_t tb = sm->tmem_base;
   const uint32_t sbase = smem_u32(base);
@@ -401,7 +420,7 @@ __device__ void role_issue_p(const Params &p, Small *sm, uint8_t *base) {
       // U^T = V^T (Tm diag beta)^T
       if (!wait1(sm, sm->t_ready, g & 1, 0x208)) { ok = false; break; }
       tc_fence_after();
-      {
+      if (kVar != kVarSplit || ui.mode != kUnitM) {  // a transition unit has v = 0: U = 0
         const uint64_t dv = dadd(d_v, s * kStageBytes);
 #pragma unroll 1
         for (int kk = 0; kk < 4; ++kk)
@@ -436,6 +455,7 @@ __device__ void role_issue_p(const Params &p, Small *sm, uint8_t *base) {
   issuer_drain(sm);
 }
 
+template <int kVar>
 __device__ void role_issue_c(const Params &p, Small *sm, uint8_t *base) {
   const uint32_t tb = sm->tmem_base;
   const uint32_t sbase = smem_u32(base);
@@ -469,8 +489,9 @@ __device__ void role_issue_c(const Params &p, Small *sm, uint8_t *base) {
       if (!wait1(sm, sm->uw_full, g & 1, 0x214)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll 1
-      for (int kk = 0; kk < 4; ++kk)
-        mma_bf16_ts(tu, tb + TM_Y + kk * 8, dadd(d_tbg, kk * 32), id_n64, 1);
+      for (int kk = 0; kk < 4; ++kk)  // (a transition unit has no U to add to)
+        mma_bf16_ts(tu, tb + TM_Y + kk * 8, dadd(d_tbg, kk * 32), id_n64,
+                    (kVar != kVarSplit || ui.mode != kUnitM || kk > 0) ? 1u : 0u);
       mma_commit(&sm->vp_full);
       // S^T += V''^T K
       if (!wait1(sm, sm->vp_ready, g & 1, 0x215)) { ok = false; break; }
@@ -784,12 +805,36 @@ __device__ __noinline__ void store_state(uint32_t taddr, float *dst, int D, int 
   }
 }
 
-// The state warpgroup.  `row` is this thread's TMEM lane = value dimension dv.  With
-// kCkpt it also writes the state checkpoints (a separate instantiation, so that the
-// plain forward's code is untouched).
+// Initial state of a split unit (row dv of S^T): zero (piece offset), the identity (piece
+// transition), or a [dk][dv] state from the split buffer; kept out of line.
+__device__ __noinline__ void state_from_split(const Params &p, uint32_t taddr, const UnitInfo &ui,
+                                              int dv) {
+  const int D = p.D;
+  const float *src = ui.mode == kUnitFinal ? p.split.states + (int64_t)ui.sin * D * D : nullptr;
+#pragma unroll 1
+  for (int cb = 0; cb < 4; ++cb) {
+    uint32_t r[32];
+#pragma unroll
+    for (int u = 0; u < 32; ++u) {
+      const int j = cb * 32 + u;
+      float x = 0.f;
+      if (j < D && dv < D) {
+        if (src) x = src[(int64_t)j * D + dv];
+        else if (ui.mode == kUnitM) x = j == dv ? 1.f : 0.f;
+      }
+      r[u] = __float_as_uint(x);
+    }
+    tmem_st32(taddr + cb * 32, r);
+  }
+  tmem_st_wait();
+}
+
+// The state warpgroup.  `row` is this thread's TMEM lane = value dimension dv.  The
+// checkpoint and split variants are separate instantiations, so that the plain
+// forward's code is untouched.
 // Per chunk: S^T -> bf16 (A operand of Y and O1) and e^{G_last} S^T; Y -> bf16;
 // V'^T -> bf16 V'^T and V''^T; and the previous chunk's output.
-template <bool kCkpt>
+template <int kVar>
 __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
   const uint32_t tb = sm->tmem_base;
   const uint32_t lane_base = (uint32_t)(row & ~31);
@@ -863,8 +908,15 @@ __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
       // the bf16 copy of S^T is rewritten once the previous chunk's O1 has read it
       if (g >= 1 && !wait_wg(sm, sm->o1_full, (g - 1) & 1, 0x408, kBarState)) { ok = false; break; }
       tc_fence_after();
-      if (c == 0) state_from_h0(p, tmem_addr(tb + TM_S, lane_base, 0), sidx, dv);
-      if constexpr (kCkpt) {
+      if (c == 0) {
+        if constexpr (kVar == kVarSplit) {
+          if (ui.mode == kUnitFull) state_from_h0(p, tmem_addr(tb + TM_S, lane_base, 0), sidx, dv);
+          else state_from_split(p, tmem_addr(tb + TM_S, lane_base, 0), ui, dv);
+        } else {
+          state_from_h0(p, tmem_addr(tb + TM_S, lane_base, 0), sidx, dv);
+        }
+      }
+      if constexpr (kVar == kVarCkpt) {
         // the state entering this chunk, after c * 64 of the segment's tokens (row chosen
         // by the producer)
         if (cv.ckrow >= 0)
@@ -944,27 +996,34 @@ __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
       tc_fence_before();
       mbar_arrive(&sm->vp_ready);
       prev_t = t;
-      prev_len = len;
+      // offset and transition units of a split segment store no output
+      prev_len = (kVar == kVarSplit && (ui.mode == kUnitR || ui.mode == kUnitM)) ? 0 : len;
       prev_head = ui.head;
     }
     if (!ok) break;
     // end of the unit: final state, then the last chunk's output
     if (!wait_wg(sm, sm->s_full, (g - 1) & 1, 0x407, kBarState)) break;
     tc_fence_after();
-    if (p.ht) {
+    if constexpr (kVar == kVarSplit) {
+      float *dst = ui.sout >= 0 ? p.split.states + (int64_t)ui.sout * D * D
+                                : (ui.sout == -1 && p.ht ? p.ht + sidx : nullptr);
+      if (dst) store_state(tmem_addr(tb + TM_S, lane_base, 0), dst, D, dv);
+    } else {
+      if (p.ht) {
 #pragma unroll 1
-      for (int cb = 0; cb < 4; ++cb) {
-        uint32_t r[32];
-        tmem_ld32(tmem_addr(tb + TM_S, lane_base, cb * 32), r);
-        tmem_ld_wait();
-        if (dv < D) {
+        for (int cb = 0; cb < 4; ++cb) {
+          uint32_t r[32];
+          tmem_ld32(tmem_addr(tb + TM_S, lane_base, cb * 32), r);
+          tmem_ld_wait();
+          if (dv < D) {
 #pragma unroll
-          for (int u = 0; u < 32; ++u)
-            if (cb * 32 + u < D) p.ht[sidx + (int64_t)(cb * 32 + u) * D + dv] = __uint_as_float(r[u]);
+            for (int u = 0; u < 32; ++u)
+              if (cb * 32 + u < D) p.ht[sidx + (int64_t)(cb * 32 + u) * D + dv] = __uint_as_float(r[u]);
+          }
         }
       }
     }
-    if constexpr (kCkpt) {
+    if constexpr (kVar == kVarCkpt) {
       const int seg_len = ui.end - ui.t0;
       if (seg_len % p.ckpt.every == 0) {
         const int64_t r = p.ckpt.off[ui.seq] + seg_len / p.ckpt.every - 1;
@@ -977,9 +1036,10 @@ __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
   }
 }
 
-// kCkpt: the variant that also writes state checkpoints (a separate kernel, so the plain
-// forward's code is not touched by it)
-template <bool kCkpt>
+// kVar: the plain forward, the variant that also writes state checkpoints, or the one
+// that runs split-segment pieces (separate kernels, so the plain forward's code is not
+// touched by the others)
+template <int kVar>
 __global__ void __launch_bounds__(kThreads, 1)
     k_fused(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
             const __grid_constant__ CUtensorMap mv, const Params p) {
@@ -1038,15 +1098,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
 
   if (warp == 0) {
-    role_producer<kCkpt>(p, sm, base, &mq, &mk, &mv);
+    role_producer<kVar>(p, sm, base, &mq, &mk, &mv);
   } else if (warp == 1) {
-    if (lane == 0) role_issue_p(p, sm, base);
+    if (lane == 0) role_issue_p<kVar>(p, sm, base);
   } else if (warp == 2) {
-    if (lane == 0) role_issue_c(p, sm, base);
+    if (lane == 0) role_issue_c<kVar>(p, sm, base);
   } else if (warp < 7) {
     role_prep(p, sm, base, 32 * (warp & 3) + lane);
   } else {
-    role_state<kCkpt>(p, sm, base, 32 * (warp & 3) + lane);
+    role_state<kVar>(p, sm, base, 32 * (warp & 3) + lane);
   }
   tc_fence_before();
   __syncthreads();
@@ -1177,10 +1237,13 @@ cudaError_t launch_fused(const FusedArgs &a, cudaStream_t stream) {
   char *w = reinterpret_cast<char *>(a.workspace);
   int32_t *counters = reinterpret_cast<int32_t *>(w);  // [0] = unit counter, [1] = n_active
   int32_t *order = reinterpret_cast<int32_t *>(w + 256);
-  k_worklist<<<1, 1024, 0, stream>>>(a.seg, a.n_seq, order, counters + 1, counters);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (a.ht && a.n_seq > 0) {
+  const bool split = a.split.units != nullptr;
+  cudaError_t e = cudaSuccess;
+  if (!split) {
+    k_worklist<<<1, 1024, 0, stream>>>(a.seg, a.n_seq, order, counters + 1, counters);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (a.ht && a.n_seq > 0 && (!split || a.split.empty_states)) {
     k_empty_states<<<a.n_seq * a.H, 256, 0, stream>>>(a.seg, a.H, a.D, a.h0, a.ht);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
@@ -1197,9 +1260,11 @@ cudaError_t launch_fused(const FusedArgs &a, cudaStream_t stream) {
     int n = 0;
     if ((e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return e;
-    if ((e = cudaFuncSetAttribute(k_fused<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(k_fused<kVarPlain>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)kSmemBytes)) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(k_fused<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        (e = cudaFuncSetAttribute(k_fused<kVarCkpt>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)kSmemBytes)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(k_fused<kVarSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)kSmemBytes)) != cudaSuccess)
       return e;
     g_num_sms[dev] = n;
@@ -1224,21 +1289,24 @@ cudaError_t launch_fused(const FusedArgs &a, cudaStream_t stream) {
   p.o_sh = a.o_sh;
   p.ht = a.ht;
   p.ckpt = a.ckpt;
+  p.split = a.split;
   p.seg = a.seg;
   p.order = order;
   p.n_active = counters + 1;
-  p.counter = counters;
+  p.counter = split ? a.split.counter : counters;
   // one CTA per SM, never more than the number of units that can exist
   int64_t units_max = (int64_t)a.H * a.n_seq;
   const int64_t by_tokens = (int64_t)a.H * ceil_div64(a.T, kChunk);
   if (by_tokens < units_max) units_max = by_tokens;
   int grid = g_num_sms[dev];
-  if (units_max < grid) grid = (int)units_max;
+  if (!split && units_max < grid) grid = (int)units_max;
   if (grid <= 0) return cudaSuccess;
-  if (p.ckpt.h)
-    k_fused<true><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+  if (split)
+    k_fused<kVarSplit><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+  else if (p.ckpt.h)
+    k_fused<kVarCkpt><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
   else
-    k_fused<false><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+    k_fused<kVarPlain><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 

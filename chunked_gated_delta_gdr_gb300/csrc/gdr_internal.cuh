@@ -84,6 +84,41 @@ cudaError_t launch_out(const StageShapes &s, View q, View k, View v_new, const v
                        View gcum, float scale, View o, const SegInfo *seg,
                        const ChunkInfo *chunks, const int32_t *n_chunks, cudaStream_t stream);
 
+// Intra-sequence split (gdr_split.cu): a long segment is cut into pieces of whole
+// chunks.  Pass A runs piece 0 from the segment's initial state (outputs and the state
+// after it) and every later piece twice: from a zero state (R, the piece's offset) and
+// from the identity with v = 0 (M, the piece's transition).  The combine step chains
+// S_{p+1} = M_p S_p + R_p; pass B runs pieces 1.. from their initial states S_p.
+enum UnitMode : int32_t { kUnitFull = 0, kUnitR = 1, kUnitM = 2, kUnitFinal = 3 };
+// state slots (`sin`, `sout`) index [D][D] fp32 blocks of SplitArgs::states;
+// sout -1: ht (if requested), -2: no state output; sin -1: h0 or zero (by mode)
+struct UnitDesc {
+  int32_t seq, head, t0, end, nch, mode, sin, sout;
+};
+struct SplitArgs {
+  const UnitDesc *units;    // null: no split (units are whole segments)
+  const int32_t *n_units;   // device count
+  float *states;            // [slots][D][D]
+  int32_t *counter;         // unit counter, zeroed by the unit builder
+  bool empty_states;        // also write ht of empty segments (pass A only)
+};
+constexpr int kSplitMaxPieces = 8;
+constexpr int kSplitMinChunks = 16;  // shortest piece worth splitting off
+// pieces per segment for U (segment, head) units on `sms` SMs (1 = do not split), and
+// the weight of the first piece against the others (`lead`)
+int split_pieces(int64_t units, int sms, int *lead);
+struct SplitWs {
+  UnitDesc *ua, *ub;
+  int32_t *na, *nb, *counters, *seg_pieces;
+  float *states;
+  size_t bytes;
+};
+SplitWs carve_split(void *ws, int32_t n_seq, int32_t H, int32_t D, int32_t pieces);
+cudaError_t launch_split_units(const SegInfo *seg, int32_t n_seq, int32_t H, int32_t pieces,
+                               int32_t lead, const SplitWs &w, cudaStream_t stream);
+cudaError_t launch_split_combine(const SplitWs &w, int32_t n_seq, int32_t H, int32_t D,
+                                 cudaStream_t stream);
+
 // Fused persistent kernel (gdr_fused.cu).
 struct FusedArgs {
   int64_t T;
@@ -100,6 +135,7 @@ struct FusedArgs {
   int64_t o_st, o_sh;
   float *ht;
   Ckpt ckpt;
+  SplitArgs split;
   const SegInfo *seg;
   void *workspace;  // fused-path scratch (work list etc.)
 };

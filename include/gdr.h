@@ -77,8 +77,15 @@ enum gdr_status {
 /* Execution paths of the forward. */
 enum gdr_path {
   GDR_PATH_AUTO = 0,   /* fused when its alignment preconditions hold, else staged */
-  GDR_PATH_FUSED = 1,  /* one persistent kernel per call; intermediates stay on chip */
-  GDR_PATH_STAGED = 2  /* the three stages as separate kernels with HBM intermediates */
+  GDR_PATH_FUSED = 1,  /* one persistent kernel per call; intermediates stay on chip.
+                          When the (segment, head) pairs are too few to fill the GPU
+                          (3 x n_seq x H <= its SM count) and no checkpoints are asked
+                          for, segments of 48 chunks or more are cut into 3 to 8
+                          pieces that run on different SMs, joined through the affine
+                          state map S_out = M S_in + R of each piece (FlashQLA's
+                          sequence split, `seq_split_idx`, "Findings ...", section 2) */
+  GDR_PATH_STAGED = 2, /* the three stages as separate kernels with HBM intermediates */
+  GDR_PATH_FUSED_WHOLE = 3 /* the fused kernel with every (segment, head) in one piece */
 };
 
 typedef struct gdr_tensor {
@@ -109,8 +116,10 @@ int gdr_chunk_fwd(const gdr_tensor_t *q, const gdr_tensor_t *k, const gdr_tensor
                   gdr_tensor_t *o, gdr_tensor_t *ht, cudaStream_t stream);
 
 /* Bytes of device scratch gdr_chunk_fwd_ws needs for these extents and path
- * (GDR_PATH_AUTO sizes for the larger of the two).  Never fails; returns 0 for
- * negative arguments. */
+ * (GDR_PATH_AUTO sizes for the larger of the two) on the current device: the
+ * fused path's sequence split depends on its SM count, and takes up to
+ * 24 x n_seq x H x dv x dv x 4 bytes for the pieces' states.  Never fails;
+ * returns 0 for negative arguments. */
 size_t gdr_chunk_fwd_workspace_bytes(int64_t T, int32_t n_seq, int32_t H, int32_t dk,
                                      int32_t dv, int32_t path);
 
@@ -156,6 +165,14 @@ int gdr_chunk_fwd_ckpt(const gdr_tensor_t *q, const gdr_tensor_t *k, const gdr_t
 /* Rows gdr_chunk_fwd_ckpt may write: floor(T / checkpoint_every_n_tokens) (0 for bad
  * arguments). */
 int64_t gdr_ckpt_count_bound(int64_t T, int32_t checkpoint_every_n_tokens);
+
+/* Pieces per segment that GDR_PATH_FUSED cuts long segments into on the current
+ * device for T tokens in n_seq segments of H value heads (1: no split; else 3..8).
+ * The first piece may weigh 2 or 3 of the others (it runs while the others' state
+ * maps are formed); a segment of c chunks gets at most floor(c / 16) - (weight - 1)
+ * pieces, and stays whole when that is under 3.  Returns 1 when no device can be
+ * queried. */
+int32_t gdr_fused_split_pieces(int64_t T, int32_t n_seq, int32_t H);
 
 /* Upper bound on the number of 64-token chunks: ceil(T / 64) + n_seq. */
 int64_t gdr_chunk_count_bound(int64_t T, int32_t n_seq);

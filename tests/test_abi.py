@@ -22,7 +22,7 @@ def _declared():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     out = {}
-    for m in re.finditer(r"\b(?:int|size_t|int64_t|const char \*)\s*\**\s*(gdr_\w+)\s*\(([^;]*?)\)\s*;",
+    for m in re.finditer(r"\b(?:int|size_t|int64_t|int32_t|const char \*)\s*\**\s*(gdr_\w+)\s*\(([^;]*?)\)\s*;",
                          src, flags=re.S):
         args = m.group(2).strip()
         n = 0 if args in ("", "void") else args.count(",") + 1
