@@ -94,11 +94,15 @@ def read_traffic(expected_sha: str):
     return traffic if (sha and sha == expected_sha) else None
 
 
+# the sources the fused forward kernel is compiled from
+KERNEL_SOURCES = ("gdr_fused.cu", "gdr_internal.cuh", "gdr_tc.cuh")
+
+
 def kernel_sha() -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "chunked_gated_delta_gdr_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
