@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for the chunked gated delta rule forward.
+"""fp64 CPU oracle for the chunked gated delta rule, forward and backward.
 
 TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 bench's CPU-baseline / reference legs may import this package.  It shares no
@@ -10,6 +10,9 @@ Two independent forms live here:
 * ``recurrent`` -- the plain definition: the gated delta rule recurrence run
   token by token in fp64 (C, OpenMP over (segment, head) units;
   ``gdr_oracle.c``).  This is the oracle the GPU path is compared with.
+* ``recurrent_bwd`` -- the gradients of ``recurrent``'s outputs with respect to
+  all its inputs, by reverse-mode differentiation of the same token recurrence
+  (C, ``gdr_oracle.c``).  Pinned by finite differences of ``recurrent``.
 * ``chunked_wy`` -- the chunkwise (WY) form in fp64 numpy, used only on tiny
   inputs to cross-check ``recurrent`` and to expose the per-chunk
   intermediates (G, A, Tm, W, U, v_new, h).
@@ -67,6 +70,11 @@ def open_library(path: str):
         ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
         ctypes.c_int32, ctypes.c_int32, vp, vp, ctypes.c_int32, vp, vp, ci]
     lib.gdr_oracle_recurrent_ckpt.restype = ci
+    lib.gdr_oracle_recurrent_bwd.argtypes = [
+        vp, ci, vp, ci, vp, ci, vp, ci, vp, ci, cd, vp, ci, vp,
+        ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+        ctypes.c_int32, ctypes.c_int32, vp, ci, vp, ci, vp, vp, vp, vp, vp, vp, ci]
+    lib.gdr_oracle_recurrent_bwd.restype = ci
     lib.gdr_oracle_max_threads.restype = ci
     return lib
 
@@ -181,3 +189,52 @@ def recurrent_checkpoints(q, k, v, g, beta, scale, h0, cu_seqlens, ckpt_every, w
     if rc != 0:
         raise RuntimeError(f"gdr_oracle_recurrent_ckpt failed with code {rc}")
     return o, ht, ckpt[:off[-1]], off
+
+
+def recurrent_bwd(q, k, v, g, beta, scale, h0, cu_seqlens, dout, dht=None, n_threads=0,
+                  lib=None):
+    """Gradients of the token recurrence (fp64) for upstream gradients ``dout``
+    (dL/do, [T, H, dv]) and ``dht`` (dL/dht, [N, H, dk, dv] or None for zero).
+
+    Returns (dq [T, Hk, dk], dk [T, Hk, dk], dv [T, H, dv], dg [T, H], dbeta [T, H],
+    dh0 [N, H, dk, dv]), all float64.  dq and dk sum the value heads that share a
+    query/key head (in head order); tokens outside every segment get zeros; dh0 is
+    returned whether or not ``h0`` is given (the gradient for a zero initial state).
+    """
+    lib = _load() if lib is None else lib
+    qa, qd = _as_np(q)
+    ka, kd = _as_np(k)
+    va, vd = _as_np(v)
+    ga, gd = _as_np(g)
+    ba, bd = _as_np(beta)
+    ha, hd = _as_np(h0)
+    da, dd = _as_np(dout)
+    ta, td = _as_np(dht)
+    try:
+        import torch
+        if isinstance(cu_seqlens, torch.Tensor):
+            cu_seqlens = cu_seqlens.cpu().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    T, Hk, dk = qa.shape
+    H, dv = va.shape[1], va.shape[2]
+    n_seq = cu.shape[0] - 1
+    dq_h = np.zeros((T, H, dk), dtype=np.float64)
+    dk_h = np.zeros((T, H, dk), dtype=np.float64)
+    dvo = np.zeros((T, H, dv), dtype=np.float64)
+    dg = np.zeros((T, H), dtype=np.float64)
+    db = np.zeros((T, H), dtype=np.float64)
+    dh0 = np.zeros((n_seq, H, dk, dv), dtype=np.float64)
+    ptr = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+    rc = lib.gdr_oracle_recurrent_bwd(
+        ptr(qa), qd, ptr(ka), kd, ptr(va), vd, ptr(ga), gd, ptr(ba), bd,
+        float(scale), ptr(ha), hd, ptr(cu), n_seq, T, Hk, H, dk, dv,
+        ptr(da), dd, ptr(ta), td, ptr(dq_h), ptr(dk_h), ptr(dvo), ptr(dg), ptr(db),
+        ptr(dh0), int(n_threads))
+    if rc != 0:
+        raise RuntimeError(f"gdr_oracle_recurrent_bwd failed with code {rc}")
+    group = H // Hk
+    dq = dq_h.reshape(T, Hk, group, dk).sum(axis=2)
+    dkk = dk_h.reshape(T, Hk, group, dk).sum(axis=2)
+    return dq, dkk, dvo, dg, db, dh0
