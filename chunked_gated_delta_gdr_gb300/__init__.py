@@ -5,10 +5,13 @@ package is its Python binding.  Importing it does not load the library; the
 first call does, and raises if the library has not been built.
 """
 from .api import (  # noqa: F401
+    bwd_workspace_bytes,
     check_cu_seqlens,
     checkpoint_count_bound,
     chunk_count_bound,
+    chunk_bwd,
     chunk_fwd,
+    chunk_gated_delta_rule,
     chunk_fwd_alloc,
     chunk_fwd_checkpoints,
     chunk_index,

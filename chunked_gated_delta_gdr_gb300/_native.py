@@ -37,6 +37,9 @@ SIGNATURES = {
                                         _vp, _sz, _vp]),
     "gdr_chunk_fwd_ckpt": (ctypes.c_int, [_T, _T, _T, _T, _T, _f32, _T, _vp, _i32, _T, _T, _T,
                                           _vp, _i32, _i32, _vp, _sz, _vp]),
+    "gdr_chunk_bwd": (ctypes.c_int, [_T, _T, _T, _T, _T, _f32, _T, _vp, _i32, _T, _T, _T, _T,
+                                     _T, _T, _T, _T, _vp, _sz, _vp]),
+    "gdr_chunk_bwd_workspace_bytes": (_sz, [_i64, _i32, _i32, _i32, _i32, _i32]),
     "gdr_ckpt_count_bound": (_i64, [_i64, _i32]),
     "gdr_fused_split_pieces": (_i32, [_i64, _i32, _i32]),
     "gdr_chunk_count_bound": (_i64, [_i64, _i32]),

@@ -127,6 +127,86 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor
     return o, ht
 
 
+def bwd_workspace_bytes(T: int, n_seq: int, Hk: int, H: int, dk: int, dv: int) -> int:
+    return int(nat.lib().gdr_chunk_bwd_workspace_bytes(T, n_seq, Hk, H, dk, dv))
+
+
+def chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+              beta: torch.Tensor, dout: torch.Tensor, scale: Optional[float] = None,
+              initial_state: Optional[torch.Tensor] = None,
+              cu_seqlens: Optional[torch.Tensor] = None, dht: Optional[torch.Tensor] = None,
+              want_dh0: bool = True, workspace: Optional[torch.Tensor] = None,
+              stream: Optional[torch.cuda.Stream] = None):
+    """Backward of ``chunk_fwd`` (libgdr ``gdr_chunk_bwd``): gradients of the loss with
+    respect to q, k, v, g, beta and the initial state, given dout = dL/do [T, H, dv] bf16
+    and dht = dL/dht [N, H, dk, dv] f32 (None: zero).
+
+    Returns (dq [T, Hk, dk], dk [T, Hk, dk], dv [T, H, dv], dg [T, H], dbeta [T, H],
+    dh0 [N, H, dk, dv] or None), all fp32 on the inputs' device.
+    """
+    dev = q.device
+    T, Hk, dk_ = q.shape
+    H, dv_ = v.shape[1], v.shape[2]
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    n_seq = cu_seqlens.numel() - 1
+    if scale is None:
+        scale = dk_ ** -0.5
+    f32 = dict(dtype=torch.float32, device=dev)
+    dq, dkk = torch.empty(T, Hk, dk_, **f32), torch.empty(T, Hk, dk_, **f32)
+    dvv, dg, db = torch.empty(T, H, dv_, **f32), torch.empty(T, H, **f32), torch.empty(T, H, **f32)
+    dh0 = torch.empty(n_seq, H, dk_, dv_, **f32) if want_dh0 else None
+    if workspace is None:
+        workspace = _workspace(bwd_workspace_bytes(T, n_seq, Hk, H, dk_, dv_), dev)
+    ins = [_Desc(t) for t in (q, k, v, g, beta)]
+    outs = [_Desc(t) for t in (dq, dkk, dvv, dg, db)]
+    d_h0, d_do, d_dht, d_dh0 = _d(initial_state), _Desc(dout), _d(dht), _d(dh0)
+    rc = nat.lib().gdr_chunk_bwd(
+        ins[0].ref, ins[1].ref, ins[2].ref, ins[3].ref, ins[4].ref, ctypes.c_float(scale),
+        _ref(d_h0), _ptr(cu_seqlens), n_seq, d_do.ref, _ref(d_dht), outs[0].ref, outs[1].ref,
+        outs[2].ref, outs[3].ref, outs[4].ref, _ref(d_dh0), ctypes.c_void_p(workspace.data_ptr()),
+        workspace.numel(), _stream(stream))
+    nat.check(rc, "gdr_chunk_bwd")
+    return dq, dkk, dvv, dg, db, dh0
+
+
+class _ChunkGatedDeltaRule(torch.autograd.Function):
+    """Autograd wrapper: the forward and backward each run in libgdr."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, g, beta, scale, initial_state, cu_seqlens, output_final_state):
+        o, ht = chunk_fwd(q, k, v, g, beta, scale=scale, initial_state=initial_state,
+                          cu_seqlens=cu_seqlens, output_final_state=output_final_state)
+        ctx.save_for_backward(q, k, v, g, beta, initial_state, cu_seqlens)
+        ctx.scale = scale
+        return o, ht
+
+    @staticmethod
+    def backward(ctx, do, dht):
+        q, k, v, g, beta, h0, cu = ctx.saved_tensors
+        dq, dk, dv, dg, db, dh0 = chunk_bwd(
+            q, k, v, g, beta, do.to(torch.bfloat16).contiguous(), scale=ctx.scale,
+            initial_state=h0, cu_seqlens=cu,
+            dht=None if dht is None else dht.float().contiguous(),
+            want_dh0=h0 is not None and ctx.needs_input_grad[6])
+        return (dq.to(q.dtype), dk.to(k.dtype), dv.to(v.dtype), dg.to(g.dtype),
+                db.to(beta.dtype), None, dh0, None, None)
+
+
+def chunk_gated_delta_rule(q, k, v, g, beta, scale: Optional[float] = None,
+                           initial_state: Optional[torch.Tensor] = None,
+                           output_final_state: bool = False,
+                           cu_seqlens: Optional[torch.Tensor] = None):
+    """Differentiable chunked gated delta rule: (o, ht) = forward, gradients through
+    ``chunk_bwd``.  Layouts as ``chunk_fwd``; device tensors only."""
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, q.shape[0]], dtype=torch.int32, device=q.device)
+    return _ChunkGatedDeltaRule.apply(q, k, v, g, beta, scale, initial_state, cu_seqlens,
+                                      output_final_state)
+
+
 def split_pieces(T: int, n_seq: int, H: int) -> int:
     """Pieces per long segment of the fused path's sequence split on the current device
     (1: the fused path runs every (segment, head) whole)."""

@@ -4,6 +4,7 @@
 #include <mutex>
 #include <string.h>
 
+#include "gdr_bwd.cuh"
 #include "gdr_internal.cuh"
 
 using namespace gdr;
@@ -422,6 +423,85 @@ int gdr_chunk_fwd(const gdr_tensor_t *q, const gdr_tensor_t *k, const gdr_tensor
   r = run_fwd(P, scale, cu_seqlens, chosen, ws, need, stream);
   if (cudaFreeAsync(ws, stream) != cudaSuccess && r == GDR_OK) r = GDR_ERR_CUDA;
   return r;
+}
+
+size_t gdr_chunk_bwd_workspace_bytes(int64_t T, int32_t n_seq, int32_t Hk, int32_t H,
+                                     int32_t dk, int32_t dv) {
+  if (T < 0 || n_seq < 0 || Hk <= 0 || H <= 0 || dk <= 0 || dv <= 0 || H % Hk) return 0;
+  const int32_t D = dk > dv ? dk : dv;
+  return carve_index(nullptr, T, n_seq).bytes + bwd_work_bytes(T, n_seq, Hk, H, D);
+}
+
+int gdr_chunk_bwd(const gdr_tensor_t *q, const gdr_tensor_t *k, const gdr_tensor_t *v,
+                  const gdr_tensor_t *g, const gdr_tensor_t *beta, float scale,
+                  const gdr_tensor_t *h0, const int32_t *cu_seqlens, int32_t n_seq,
+                  const gdr_tensor_t *dout, const gdr_tensor_t *dht, gdr_tensor_t *dq,
+                  gdr_tensor_t *dk, gdr_tensor_t *dv, gdr_tensor_t *dg, gdr_tensor_t *dbeta,
+                  gdr_tensor_t *dh0, void *workspace, size_t workspace_bytes,
+                  cudaStream_t stream) {
+  Problem P;
+  // dout is checked as the forward's o, dht as its ht
+  int r = validate_fwd(q, k, v, g, beta, h0, cu_seqlens, n_seq, dout, dht, &P);
+  if (r) return r;
+  Desc Dq, Dk, Dv, Dg, Db, Dh;
+  const int64_t qs[3] = {P.T, P.Hk, P.D}, vs[3] = {P.T, P.H, P.D}, gs[2] = {P.T, P.H};
+  if ((r = read_desc(dq, GDR_F32, 3, &Dq)) || (r = read_desc(dk, GDR_F32, 3, &Dk)) ||
+      (r = read_desc(dv, GDR_F32, 3, &Dv)) || (r = read_desc(dg, GDR_F32, 2, &Dg)) ||
+      (r = read_desc(dbeta, GDR_F32, 2, &Db)))
+    return r;
+  for (int i = 0; i < 3; ++i)
+    if (Dq.shape[i] != qs[i] || Dk.shape[i] != qs[i] || Dv.shape[i] != vs[i]) return GDR_ERR_SHAPE;
+  for (int i = 0; i < 2; ++i)
+    if (Dg.shape[i] != gs[i] || Db.shape[i] != gs[i]) return GDR_ERR_SHAPE;
+  if (!compact(Dq) || !compact(Dk) || !compact(Dv) || !compact(Dg) || !compact(Db))
+    return GDR_ERR_STRIDE;
+  if (dh0) {
+    if ((r = read_desc(dh0, GDR_F32, 4, &Dh))) return r;
+    if (Dh.shape[0] != n_seq) return GDR_ERR_NSEQ;
+    if (Dh.shape[1] != P.H || Dh.shape[2] != P.D || Dh.shape[3] != P.D) return GDR_ERR_SHAPE;
+    if (!compact(Dh)) return GDR_ERR_STRIDE;
+  }
+  if ((r = device_ok())) return r;
+  if (P.n_seq == 0) return GDR_OK;
+  const size_t need = gdr_chunk_bwd_workspace_bytes(P.T, P.n_seq, P.Hk, P.H, P.D, P.D);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return GDR_ERR_WORKSPACE;
+  // tokens outside every segment keep zero gradients
+  const size_t tq = sizeof(float) * (size_t)P.T * P.Hk * P.D;
+  const size_t tv = sizeof(float) * (size_t)P.T * P.H * P.D, tg = sizeof(float) * (size_t)P.T * P.H;
+  if (cudaMemsetAsync(Dq.p, 0, tq, stream) != cudaSuccess ||
+      cudaMemsetAsync(Dk.p, 0, tq, stream) != cudaSuccess ||
+      cudaMemsetAsync(Dv.p, 0, tv, stream) != cudaSuccess ||
+      cudaMemsetAsync(Dg.p, 0, tg, stream) != cudaSuccess ||
+      cudaMemsetAsync(Db.p, 0, tg, stream) != cudaSuccess)
+    return GDR_ERR_CUDA;
+  const IndexWs ix = carve_index(workspace, P.T, P.n_seq);
+  const int64_t cap = chunk_bound(P.T, P.n_seq);
+  if (launch_chunk_index(cu_seqlens, P.n_seq, P.T, ix.seg, ix.chunks, cap, ix.n_chunks,
+                         stream) != cudaSuccess)
+    return GDR_ERR_CUDA;
+  BwdArgs a{};
+  a.s = StageShapes{P.T, P.n_seq, P.Hk, P.H, P.D, cap};
+  a.q = view_of(P.q);
+  a.k = view_of(P.k);
+  a.v = view_of(P.v);
+  a.g = view_of(P.g);
+  a.beta = view_of(P.beta);
+  a.dout = view_of(P.o);
+  a.h0 = P.has_h0 ? reinterpret_cast<const float *>(P.h0.p) : nullptr;
+  a.dht = P.has_ht ? reinterpret_cast<const float *>(P.ht.p) : nullptr;
+  a.scale = scale;
+  a.dq = view_of(Dq);
+  a.dk = view_of(Dk);
+  a.dv = view_of(Dv);
+  a.dg = view_of(Dg);
+  a.dbeta = view_of(Db);
+  a.dh0 = dh0 ? reinterpret_cast<float *>(Dh.p) : nullptr;
+  a.seg = ix.seg;
+  a.chunks = ix.chunks;
+  a.n_chunks = ix.n_chunks;
+  a.work = reinterpret_cast<char *>(workspace) + ix.bytes;
+  return launch_bwd(a, stream) == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 
 int gdr_chunk_index(const int32_t *cu_seqlens, int32_t n_seq, int64_t T, int32_t *seg_table,

@@ -174,6 +174,44 @@ int64_t gdr_ckpt_count_bound(int64_t T, int32_t checkpoint_every_n_tokens);
  * queried. */
 int32_t gdr_fused_split_pieces(int64_t T, int32_t n_seq, int32_t H);
 
+/*
+ * gdr_chunk_bwd -- the backward: gradients of gdr_chunk_fwd's outputs with respect to
+ * all its inputs.  FlashQLA's GDN kernels serve as a training backend whose backward
+ * is bit-reproducible and tolerates length-0 segments ("Findings ...", intro and
+ * section 2); the pages print no backward formula, so this is the gradient of the
+ * forward defined above (its chunk form is written out in gdr_bwd.cu).
+ *
+ *   q, k, v, g, beta, scale, h0, cu_seqlens, n_seq
+ *           the forward's inputs, as gdr_chunk_fwd takes them (the forward is
+ *           recomputed from them; nothing of a previous forward call is kept)
+ *   dout    [T, H, dv] bf16, dL/do (read for covered tokens only)
+ *   dht     [n_seq, H, dk, dv] f32 compact, dL/dht, or NULL for zero
+ *   dq, dk  [T, Hk, dk] f32 compact out (grouped heads: summed over the value heads
+ *           that share a query/key head, in head order)
+ *   dv      [T, H, dv] f32 compact out
+ *   dg, dbeta  [T, H] f32 compact out
+ *   dh0     [n_seq, H, dk, dv] f32 compact out, or NULL to skip: the gradient for the
+ *           initial state (h0 or the zero state); an empty segment's dh0 is its dht
+ *   workspace   device, 256-byte aligned, >= gdr_chunk_bwd_workspace_bytes(...) bytes
+ *
+ * Tokens outside every segment get zero gradients.  Deterministic: every output
+ * element is written by one thread per kernel in a fixed order (no atomics), so
+ * results are bit-identical from run to run.  Stream-ordered, no host synchronisation.
+ * Errors: as gdr_chunk_fwd_ws (dout is checked like o, dht like ht), GDR_ERR_STRIDE
+ * for non-compact outputs, GDR_ERR_WORKSPACE.
+ */
+int gdr_chunk_bwd(const gdr_tensor_t *q, const gdr_tensor_t *k, const gdr_tensor_t *v,
+                  const gdr_tensor_t *g, const gdr_tensor_t *beta, float scale,
+                  const gdr_tensor_t *h0, const int32_t *cu_seqlens, int32_t n_seq,
+                  const gdr_tensor_t *dout, const gdr_tensor_t *dht, gdr_tensor_t *dq,
+                  gdr_tensor_t *dk, gdr_tensor_t *dv, gdr_tensor_t *dg, gdr_tensor_t *dbeta,
+                  gdr_tensor_t *dh0, void *workspace, size_t workspace_bytes,
+                  cudaStream_t stream);
+
+/* Bytes of device scratch gdr_chunk_bwd needs (0 for bad arguments). */
+size_t gdr_chunk_bwd_workspace_bytes(int64_t T, int32_t n_seq, int32_t Hk, int32_t H,
+                                     int32_t dk, int32_t dv);
+
 /* Upper bound on the number of 64-token chunks: ceil(T / 64) + n_seq. */
 int64_t gdr_chunk_count_bound(int64_t T, int32_t n_seq);
 

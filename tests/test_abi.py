@@ -217,3 +217,55 @@ def test_checkpoint_count_bound(lib):
     assert lib.gdr_ckpt_count_bound(1000, 64) == 15
     assert lib.gdr_ckpt_count_bound(1000, 0) == 0
     assert lib.gdr_ckpt_count_bound(-1, 64) == 0
+
+
+def _call_bwd(lib, a, outs, ws=0x40000, ws_bytes=1 << 40):
+    r = lambda d: None if d is None else ctypes.byref(d)
+    return lib.gdr_chunk_bwd(r(a["q"]), r(a["k"]), r(a["v"]), r(a["g"]), r(a["beta"]),
+                             ctypes.c_float(0.125), r(a["h0"]), a["cu"], a["n_seq"], r(a["o"]),
+                             r(a["ht"]), r(outs["dq"]), r(outs["dk"]), r(outs["dv"]),
+                             r(outs["dg"]), r(outs["dbeta"]), r(outs["dh0"]), ctypes.c_void_p(ws),
+                             ws_bytes, None)
+
+
+@pytest.mark.parametrize("case,code", [
+    ("dout_dtype", -2), ("dq_dtype", -2), ("dq_heads", -3), ("dv_rows", -3), ("dg_rank", -3),
+    ("dbeta_noncompact", -4), ("dh0_nseq", -7), ("dh0_dim", -3), ("dk_null", -1),
+    ("dht_noncompact", -4),
+])
+def test_backward_validation_errors(lib, case, code):
+    # the backward checks dout like the forward's o and dht like its ht, and its fp32
+    # outputs for shape, type and compactness, before touching the device
+    f = _Fake()
+    T, Hk, H, D, N = f.T, f.Hk, f.H, f.D, f.N
+    F = nat.GDR_F32
+    outs = dict(dq=f.t([T, Hk, D], F), dk=f.t([T, Hk, D], F), dv=f.t([T, H, D], F),
+                dg=f.t([T, H], F), dbeta=f.t([T, H], F), dh0=f.t([N, H, D, D], F))
+    over = {}
+    if case == "dout_dtype":
+        over = dict(o=f.t([T, H, D], F))
+    elif case == "dht_noncompact":
+        over = dict(ht=f.t([N, H, D, D], F, strides=[2 * H * D * D, D * D, D, 1]))
+    outs.update({
+        "dq_dtype": dict(dq=f.t([T, Hk, D], nat.GDR_BF16)),
+        "dq_heads": dict(dq=f.t([T, H, D], F)),
+        "dv_rows": dict(dv=f.t([T - 1, H, D], F)),
+        "dg_rank": dict(dg=f.t([T, H, 1], F)),
+        "dbeta_noncompact": dict(dbeta=f.t([T, H], F, strides=[2 * H, 1])),
+        "dh0_nseq": dict(dh0=f.t([N + 1, H, D, D], F)),
+        "dh0_dim": dict(dh0=f.t([N, H, D, D + 1], F)),
+        "dk_null": dict(dk=None),
+    }.get(case, {}))
+    rc = _call_bwd(lib, f.args(**over), outs)
+    assert rc == code, (case, rc)
+
+
+def test_backward_workspace_bytes(lib):
+    T, N, Hk, H, D = 1000, 3, 2, 4, 64
+    b = lib.gdr_chunk_bwd_workspace_bytes(T, N, Hk, H, D, D)
+    # at least the fp32 per-token gradient scratch (dV', dW and the per-value-head dq, dk)
+    assert b >= 4 * T * H * D * 4
+    assert lib.gdr_chunk_bwd_workspace_bytes(T, N, 3, 4, D, D) == 0  # H not a multiple of Hk
+    assert lib.gdr_chunk_bwd_workspace_bytes(-1, N, Hk, H, D, D) == 0
+    # one value head per key head needs no per-value-head scratch
+    assert lib.gdr_chunk_bwd_workspace_bytes(T, N, H, H, D, D) < b

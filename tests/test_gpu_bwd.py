@@ -1,0 +1,153 @@
+"""GPU parity of the backward (``gdr_chunk_bwd``) against the fp64 oracle's backward.
+
+The pages describe FlashQLA's GDN kernels as a training backend with a bit-reproducible
+backward that tolerates length-0 segments ("Findings from integrating FlashQLA's
+Blackwell GDN kernels into a JAX trainer", intro and section 2), and state no gradient
+tolerance.  The tolerance here follows from the arithmetic: the backward recomputes the
+forward's chunk states S_0, V', W and U rounded to bf16 as the forward stores them,
+and each gradient is a chain of a few products of such operands (about five roundings
+of 2^-9 relative each) with fp32 accumulation, so every gradient tensor is compared by
+max |delta| / max |ref| <= 2e-2 (about 2x that bound) and cosine >= 0.9995 over covered
+tokens.  dh0 uses the same bound.  Results must be bit-identical from run to run.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from chunked_gated_delta_gdr_gb300 import api
+from chunked_gated_delta_gdr_gb300.inputs import make_named, make_workload
+from gdr_testlib import covered_tokens
+
+pytestmark = pytest.mark.gpu
+
+REL = 2e-2
+COS = 0.9995
+
+# lengths (zeros allowed), Hk, H, d, with h0 and dht
+CASES = {
+    "d64_ragged_gqa": ([150, 0, 64, 1, 200], 2, 4, 64, True),
+    "d128_h0": ([300, 129], 1, 2, 128, True),
+    "d128_no_state": ([256], 2, 2, 128, False),
+}
+
+
+def _upstream(w, seed, with_dht):
+    gen = torch.Generator().manual_seed(seed)
+    do = (0.1 * torch.randn(w.T, w.H, w.dv, generator=gen)).to(torch.bfloat16)
+    dht = (0.1 * torch.randn(w.n_seq, w.H, w.dk, w.dv, generator=gen)) if with_dht else None
+    return do, dht
+
+
+def _run_bwd(w, do, dht):
+    wd = w.to("cuda")
+    out = api.chunk_bwd(wd.q, wd.k, wd.v, wd.g, wd.beta, do.cuda(), scale=w.scale,
+                        initial_state=wd.h0, cu_seqlens=wd.cu_seqlens,
+                        dht=None if dht is None else dht.cuda(), want_dh0=True)
+    torch.cuda.synchronize()
+    return out
+
+
+def _oracle_bwd(w, do, dht, heads=None):
+    if heads is None:
+        return oracle.recurrent_bwd(w.q, w.k, w.v, w.g, w.beta, w.scale, w.h0, w.cu_seqlens, do,
+                                    dht)
+    # a subset of value heads (whole query/key groups)
+    group = w.H // w.Hk
+    hk = sorted({h // group for h in heads})
+    hv = [hh for g_ in hk for hh in range(g_ * group, (g_ + 1) * group)]
+    sel = lambda t, idx: t[:, idx].contiguous()
+    h0 = None if w.h0 is None else w.h0[:, hv].contiguous()
+    return oracle.recurrent_bwd(sel(w.q, hk), sel(w.k, hk), sel(w.v, hv), sel(w.g, hv),
+                                sel(w.beta, hv), w.scale, h0, w.cu_seqlens, sel(do, hv),
+                                None if dht is None else dht[:, hv].contiguous()), hk, hv
+
+
+def _close(name, got, ref, mask=None):
+    a = got.float().cpu().numpy().astype(np.float64)
+    b = np.asarray(ref, dtype=np.float64)
+    if mask is not None:
+        a, b = a[mask], b[mask]
+    scale = max(float(np.abs(b).max()), 1e-30)
+    rel = float(np.abs(a - b).max()) / scale
+    cos = float((a * b).sum() / (np.linalg.norm(a) * np.linalg.norm(b) + 1e-300))
+    assert rel <= REL, f"{name}: max|delta|/max|ref| {rel:.3e} > {REL}"
+    assert cos >= COS, f"{name}: cosine {cos:.6f} < {COS}"
+    return rel, cos
+
+
+NAMES = ("dq", "dk", "dv", "dg", "dbeta", "dh0")
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_backward_against_oracle(case):
+    lens, Hk, H, d, state = CASES[case]
+    w = make_workload(case, 23, lens, Hk, H, d, with_h0=state)
+    do, dht = _upstream(w, 24, state)
+    got = _run_bwd(w, do, dht)
+    ref = oracle.recurrent_bwd(w.q, w.k, w.v, w.g, w.beta, w.scale, w.h0, w.cu_seqlens, do, dht)
+    mask = covered_tokens(w.cu_seqlens, w.T)
+    for name, a, b in zip(NAMES, got, ref):
+        _close(name, a, b, None if name == "dh0" else mask)
+    # tokens outside every segment: none here; empty segments hand dht back as dh0
+    for n, (s, e) in enumerate(zip(w.cu_seqlens[:-1].tolist(), w.cu_seqlens[1:].tolist())):
+        if s == e:
+            want = torch.zeros_like(got[5][n]) if dht is None else dht[n].cuda()
+            assert torch.equal(got[5][n], want)
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_backward_bit_identical_run_to_run(case):
+    lens, Hk, H, d, state = CASES[case]
+    w = make_workload(case, 23, lens, Hk, H, d, with_h0=state)
+    do, dht = _upstream(w, 24, state)
+    a = _run_bwd(w, do, dht)
+    b = _run_bwd(w, do, dht)
+    for name, x, y in zip(NAMES, a, b):
+        assert torch.equal(x, y), name
+
+
+def test_backward_ghost_segments_change_nothing():
+    # trailing length-0 segments (as a static-shape caller pads cu_seqlens) leave every
+    # gradient of the real tokens bit-identical
+    w = make_workload("ghosts", 31, [200, 77], 1, 2, 64, with_h0=True)
+    do, dht = _upstream(w, 32, True)
+    a = _run_bwd(w, do, dht)
+    w2 = make_workload("ghosts", 31, [200, 77, 0, 0, 0], 1, 2, 64, with_h0=True)
+    w2.q, w2.k, w2.v, w2.g, w2.beta = w.q, w.k, w.v, w.g, w.beta
+    w2.h0 = torch.cat([w.h0, torch.randn(3, 2, 64, 64)])
+    dht2 = torch.cat([dht, torch.randn(3, 2, 64, 64)])
+    b = _run_bwd(w2, do, dht2)
+    for name, x, y in zip(NAMES[:5], a[:5], b[:5]):
+        assert torch.equal(x, y), name
+    assert torch.equal(a[5], b[5][:2])
+    assert torch.equal(b[5][2:], dht2[2:].cuda())
+
+
+def test_autograd_wrapper_matches_chunk_bwd():
+    w = make_workload("autograd", 41, [130, 70], 1, 2, 64, with_h0=True)
+    do, dht = _upstream(w, 42, True)
+    wd = w.to("cuda")
+    leaves = [t.clone().requires_grad_(True) for t in (wd.q, wd.k, wd.v, wd.g, wd.beta, wd.h0)]
+    o, ht = api.chunk_gated_delta_rule(*leaves[:5], scale=w.scale, initial_state=leaves[5],
+                                       output_final_state=True, cu_seqlens=wd.cu_seqlens)
+    ((o.float() * do.cuda().float()).sum() + (ht * dht.cuda()).sum()).backward()
+    ref = _run_bwd(w, do, dht)
+    for leaf, r, name in zip(leaves, ref, NAMES):
+        assert torch.equal(leaf.grad, r.to(leaf.dtype)), name
+
+
+@pytest.mark.slow
+def test_backward_full_size_packed_sampled_heads():
+    # the packed 64k-token workload (H = 32, d = 128, 16 trailing ghosts), value heads 0
+    # and 31 against the oracle
+    w = make_named("packed_64k_h32")
+    do, dht = _upstream(w, 51, False)
+    got = _run_bwd(w, do, dht)
+    (ref, hk, hv) = _oracle_bwd(w, do, dht, heads=[0, 31])
+    mask = covered_tokens(w.cu_seqlens, w.T)
+    _close("dq", got[0][:, hk], ref[0], mask)
+    _close("dk", got[1][:, hk], ref[1], mask)
+    for name, i in (("dv", 2), ("dg", 3), ("dbeta", 4)):
+        _close(name, got[i][:, hv], ref[i], mask)
+    _close("dh0", got[5][:, hv], ref[5])
