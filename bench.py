@@ -36,6 +36,8 @@ def parse():
     p.add_argument("--steps", type=int, default=100)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--op", choices=["fwd", "bwd"], default="fwd",
+                   help="fwd: the forward (the headline); bwd: the backward")
     p.add_argument("--path", choices=["auto", "fused", "staged", "fused_whole"], default="auto")
     p.add_argument("--workload", default=WORKLOAD)
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -394,8 +396,213 @@ def bench_e2e(args, api, w, dev, path, dist):
             "timed": "host wall clock around the public chunk_fwd call on pinned host tensors"}
 
 
+METRIC_BWD = "GDR chunk-bwd tokens/s (H=32, d=128, 64k packed) & % of fp32 SIMT roofline"
+SM_COUNT, FP32_LANES_PER_SM = 152, 128
+
+
+def algorithmic_flops_bwd(w) -> int:
+    """Per chunk of c tokens and value head: the dense products of the chunk backward
+    (6 c d^2 + 12 c^2 d + 2 c^3 multiply-adds: dV', dS_0, dQ, dK, dW, E, T^T dU, T^T dW,
+    dT, dA, B K) plus the forward recompute (the forward's 5 c^2 d + 3 c d^2)."""
+    d = w.dk
+    cu = [int(x) for x in w.cu_seqlens.tolist()]
+    tot = 0
+    for s, e in zip(cu[:-1], cu[1:]):
+        L = max(e - s, 0)
+        for c0 in range(0, L, 64):
+            c = min(64, L - c0)
+            tot += 2 * (9 * c * d * d + 17 * c * c * d + 2 * c ** 3)
+    return tot * w.H
+
+
+def algorithmic_bytes_bwd(w) -> int:
+    """Reads q, k, v, dout (bf16), g (fp32), beta (bf16), h0 and dht (fp32, if present);
+    writes dq, dk, dv, dg, dbeta (fp32) and dh0 (fp32, if h0 is given)."""
+    T, Hk, H, dk, dv = w.T, w.Hk, w.H, w.dk, w.dv
+    b = T * (2 * dk * Hk * 2 + 2 * dv * H * 2 + 4 * H + 2 * H)
+    b += T * (2 * dk * Hk * 4 + dv * H * 4 + 8 * H)
+    states = w.n_seq * H * dk * dv * 4
+    b += states * ((w.h0 is not None) * 2 + bool(w.want_ht))
+    return b
+
+
+def fp32_simt_peak_tflops(sm_mhz: float) -> float:
+    """152 SMs x 128 FP32 lanes x 2 FLOP per FMA x the SM clock."""
+    return SM_COUNT * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+
+
+def _upstream_bwd(w, dev):
+    import torch
+    gen = torch.Generator().manual_seed(4321)
+    do = (0.1 * torch.randn(w.T, w.H, w.dv, generator=gen)).to(torch.bfloat16)
+    dht = (0.1 * torch.randn(w.n_seq, w.H, w.dk, w.dv, generator=gen)) if w.want_ht else None
+    return do, dht
+
+
+def bench_ours_bwd(args):
+    import torch
+    dist, rank, ws = dist_setup(args)
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from chunked_gated_delta_gdr_gb300 import api
+    from chunked_gated_delta_gdr_gb300.inputs import make_named
+    w = make_named(args.workload)
+    wd = w.to(dev)
+    do_h, dht_h = _upstream_bwd(w, dev)
+    do, dht = do_h.to(dev), None if dht_h is None else dht_h.to(dev)
+    want_dh0 = w.h0 is not None
+    work = torch.empty(max(api.bwd_workspace_bytes(w.T, w.n_seq, w.Hk, w.H, w.dk, w.dv), 256),
+                       dtype=torch.uint8, device=dev)
+
+    def step():
+        return api.chunk_bwd(wd.q, wd.k, wd.v, wd.g, wd.beta, do, scale=w.scale,
+                             initial_state=wd.h0, cu_seqlens=wd.cu_seqlens, dht=dht,
+                             want_dh0=want_dh0, workspace=work)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_wall = time.perf_counter()
+    for a, b in ev:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    per = [a.elapsed_time(b) for a, b in ev]
+    total_ms = max_over_ranks(sum(per), dist, dev)
+    med_ms = statistics.median(per)
+    flops = algorithmic_flops_bwd(w)
+    byts = algorithmic_bytes_bwd(w)
+    sm_mhz = (clocks or {}).get("sm_max_mhz") or 2070.0
+    peak = fp32_simt_peak_tflops(sm_mhz)
+    hbm, _, peak_kind = peaks()
+    achieved = flops / (med_ms / 1e3) / 1e12
+    # chunk enumeration (2), forward recompute (2), five backward kernels, grouped heads
+    launches = 2 + 2 + 5 + (w.H != w.Hk)
+    line = {"metric": METRIC_BWD, "value": job_tokens_per_s(ws, w.T, args.steps, total_ms),
+            "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "op": "backward", "T": w.T, "H": w.H, "Hk": w.Hk,
+                       "d": w.dk, "n_seq": w.n_seq, "n_chunks": w.n_chunks(),
+                       "upstream": "dout = 0.1 N(0,1) bf16" + (", dht = 0.1 N(0,1)" if dht is not None else ""),
+                       "l2": "inputs and fp32 gradients exceed the 129 MB L2; no flush between steps"},
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak,
+                         "peak_kind": "derived: 152 SMs x 128 FP32 lanes x 2 FLOP x SM clock",
+                         "traffic": None, "algorithmic_flops_per_launch": flops,
+                         "hbm": {"algorithmic_bytes_per_launch": byts,
+                                 "achieved_gbs": byts / (med_ms / 1e3) / 1e9, "peak": hbm,
+                                 "peak_kind": f"{peak_kind} burst copy"},
+                         "timed": "median CUDA-event time of the whole backward call per step"},
+            "gpu_launches": launches * args.steps, "clocks": clocks,
+            "wall_s_timed_region": wall}
+    if not args.no_e2e:
+        hs = [t.pin_memory() for t in (w.q, w.k, w.v, w.g, w.beta, do_h)]
+        hh0 = None if w.h0 is None else w.h0.pin_memory()
+        hdht = None if dht_h is None else dht_h.pin_memory()
+
+        def step_host():
+            return api.chunk_bwd(*hs, scale=w.scale, initial_state=hh0, cu_seqlens=w.cu_seqlens,
+                                 dht=hdht, want_dh0=want_dh0, workspace=work)
+
+        step_host()
+        torch.cuda.synchronize()
+        n = max(3, min(args.steps, 5))
+        t0 = time.perf_counter()
+        for _ in range(n):
+            outs = step_host()
+        el = max_over_ranks(time.perf_counter() - t0, dist, dev)
+        h2d = sum(t.numel() * t.element_size() for t in hs + [hh0, hdht, w.cu_seqlens]
+                  if t is not None)
+        d2h = sum(t.numel() * t.element_size() for t in outs if t is not None)
+        line["e2e"] = {"value": ws * w.T * n / el, "unit": "tokens/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+                       "timed": "host wall clock around the public chunk_bwd call on pinned "
+                                "host tensors"}
+    if rank == 0 and not args.no_cpu_baseline and ws == 1:
+        line["cpu_baseline"] = cpu_oracle_bwd_sample(w, do_h, dht_h, args.cpu_seconds)
+    if dist is not None:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def _oracle_bwd_heads(w, do, dht, heads):
+    import oracle
+    hk = [h // (w.H // w.Hk) for h in heads]
+    sel = lambda t: t[:, heads].contiguous()
+    t0 = time.perf_counter()
+    # one value head per key head taken: the key heads are selected alongside
+    oracle.recurrent_bwd(w.q[:, hk].contiguous(), w.k[:, hk].contiguous(), sel(w.v), sel(w.g),
+                         sel(w.beta), w.scale, None if w.h0 is None else sel(w.h0),
+                         w.cu_seqlens, sel(do), None if dht is None else sel(dht))
+    return time.perf_counter() - t0
+
+
+def cpu_oracle_bwd_sample(w, do, dht, target_s: float):
+    """Time the fp64 oracle's backward on a head subset of the workload (~target_s)."""
+    import oracle
+    t1 = _oracle_bwd_heads(w, do, dht, [0])
+    nh = max(1, min(w.H, int(target_s / max(t1, 1e-3))))
+    el = _oracle_bwd_heads(w, do, dht, list(range(nh)))
+    return {"value": w.T * nh / w.H / el, "unit": "tokens/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"fp64 backward of the token recurrence on {nh} of {w.H} heads of the "
+                      f"full {w.name} workload ({w.T} tokens), {el:.1f} s; tokens/s scaled by "
+                      f"{nh}/{w.H}"}
+
+
+def bench_reference_bwd(args):
+    dist, rank, ws = dist_setup(args)
+    if rank != 0:
+        return 0
+    from chunked_gated_delta_gdr_gb300.inputs import make_named
+    import oracle
+    w = make_named(args.workload)
+    do, dht = _upstream_bwd(w, None)
+    times = []
+    for i in range(args.warmup + args.steps):
+        el = _oracle_bwd_heads(w, do, dht, [i % w.H])
+        if i >= args.warmup:
+            times.append(el)
+    per_step = sum(times) / len(times)
+    value = w.T / w.H / per_step
+    line = {"impl": "reference", "metric": METRIC_BWD, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "op": "backward", "T": w.T, "H": w.H, "Hk": w.Hk,
+                       "d": w.dk, "n_seq": w.n_seq, "step": "one value head of the workload"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.max_threads(),
+                             "kind": "oracle",
+                             "sample": "each step runs the fp64 backward on one of the "
+                                       f"{w.H} heads; tokens/s scaled by 1/{w.H}"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
+    if args.op == "bwd":
+        return bench_reference_bwd(args) if args.impl == "reference" else bench_ours_bwd(args)
     if args.impl == "reference":
         return bench_reference(args)
     return bench_ours(args)

@@ -142,8 +142,25 @@ def chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor
     and dht = dL/dht [N, H, dk, dv] f32 (None: zero).
 
     Returns (dq [T, Hk, dk], dk [T, Hk, dk], dv [T, H, dv], dg [T, H], dbeta [T, H],
-    dh0 [N, H, dk, dv] or None), all fp32 on the inputs' device.
+    dh0 [N, H, dk, dv] or None), all fp32 on the inputs' device.  Host (CPU) inputs are
+    copied to the current CUDA device, and the gradients back into pinned host tensors.
     """
+    if q.device.type == "cpu":
+        dev = torch.device("cuda", torch.cuda.current_device())
+        mv = lambda t: None if t is None else t.to(dev, non_blocking=True)
+        res = chunk_bwd(*map(mv, (q, k, v, g, beta, dout)), scale=scale,
+                        initial_state=mv(initial_state), cu_seqlens=mv(cu_seqlens), dht=mv(dht),
+                        want_dh0=want_dh0, workspace=workspace, stream=stream)
+        outs = []
+        for t in res:
+            if t is None:
+                outs.append(None)
+                continue
+            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            h.copy_(t, non_blocking=True)
+            outs.append(h)
+        torch.cuda.current_stream().synchronize()
+        return tuple(outs)
     dev = q.device
     T, Hk, dk_ = q.shape
     H, dv_ = v.shape[1], v.shape[2]
