@@ -1,5 +1,6 @@
 // gdr_bwd.cu -- backward of the chunked gated delta rule: dq, dk, dv, dg, dbeta, dh0 from
-// dL/do and dL/dht.  Plain fp32 SIMT arithmetic over shared-memory tiles.
+// dL/do and dL/dht.  fp32 shared-memory tiles; the dense products run on the tensor
+// pipe as warp tiles (tf32 in, fp32 accumulate, gdr_mma.cuh), the rest in fp32 SIMT.
 //
 // The pages describe a training backend whose backward is bit-reproducible and
 // tolerates length-0 segments ("Findings from integrating FlashQLA's Blackwell GDN
@@ -35,6 +36,7 @@
 // Every output element is written by one thread per kernel, in a fixed order: the
 // result is bit-identical from run to run (no atomics).
 #include "gdr_bwd.cuh"
+#include "gdr_mma.cuh"
 
 namespace gdr {
 namespace {
@@ -42,57 +44,52 @@ namespace {
 // ---------------------------------------------------------------- dV' intra part
 template <int D>
 struct DvIntraSmem {
-  static constexpr int kLd = D + 1;
-  static constexpr size_t bytes = sizeof(float) * (2 * 64 * kLd + 2 * 64 * 65 + 64);
+  static constexpr int kLd = ld_rows(D), kLdP = ld_cols(64);
+  static constexpr size_t bytes = sizeof(float) * (2 * 64 * kLd + 2 * 64 * kLdP + 64);
 };
 
 template <int D>
 __global__ void __launch_bounds__(256)
     k_bwd_dv_intra(int32_t group, View q, View k, View dout, View gcum, float scale, View dvp,
-                   const ChunkInfo *__restrict__ chunks, const int32_t *__restrict__ n_chunks) {
+                   const ChunkInfo *__restrict__ chunks, const int32_t *__restrict__ n_chunks,
+                   bool vec) {
   extern __shared__ float sm[];
-  constexpr int L = DvIntraSmem<D>::kLd;
+  constexpr int L = DvIntraSmem<D>::kLd, LP = DvIntraSmem<D>::kLdP;
   const int cid = blockIdx.x, h = blockIdx.y, cb = blockIdx.z * 64, tid = threadIdx.x;
   if (cid >= *n_chunks) return;
   const ChunkInfo ci = chunks[cid];
   const int len = ci.len, hk = h / group;
   const int64_t t0 = ci.start;
-  float *Qs = sm, *Ks = Qs + 64 * L, *Ds = Ks + 64 * L, *P = Ds + 64 * 65, *G = P + 64 * 65;
-  for (int idx = tid; idx < 64 * D; idx += blockDim.x) {
-    const int i = idx / D, d = idx % D;
-    float qv = 0.f, kv = 0.f;
-    if (i < len) {
-      qv = ldbf(q.p, (t0 + i) * q.st + hk * q.sh + d);
-      kv = ldbf(k.p, (t0 + i) * k.st + hk * k.sh + d);
-    }
-    Qs[i * L + d] = qv;
-    Ks[i * L + d] = kv;
-  }
-  for (int idx = tid; idx < 64 * 64; idx += blockDim.x) {
-    const int i = idx / 64, c = idx % 64;
-    Ds[i * 65 + c] = i < len ? ldbf(dout.p, (t0 + i) * dout.st + h * dout.sh + cb + c) : 0.f;
-  }
+  float *Qs = sm, *Ks = Qs + 64 * L, *Ds = Ks + 64 * L, *P = Ds + 64 * LP, *G = P + 64 * LP;
+  tile_bf16<64, D, 256>(Qs, L, bf_row(q, t0, hk), q.st, len, vec);
+  tile_bf16<64, D, 256>(Ks, L, bf_row(k, t0, hk), k.st, len, vec);
+  tile_bf16<64, 64, 256>(Ds, LP, bf_row(dout, t0, h) + cb, dout.st, len, vec);
   if (tid < 64) G[tid] = tid < len ? ldf(gcum.p, (t0 + tid) * gcum.st + h * gcum.sh) : 0.f;
   __syncthreads();
-  for (int idx = tid; idx < 64 * 64; idx += blockDim.x) {
-    const int i = idx / 64, j = idx % 64;
-    float pv = 0.f;
-    if (j <= i && i < len) {
-      float dot = 0.f;
-#pragma unroll 8
-      for (int d = 0; d < D; ++d) dot += Qs[i * L + d] * Ks[j * L + d];
-      pv = expf(G[i] - G[j]) * dot;
+  const int warp = tid >> 5;
+  // P = (Q K^T) o Gam (j <= i): 32 tiles of 16 x 8, four per warp
+  for (int tl = warp * 4; tl < warp * 4 + 4; ++tl) {
+    const int m0 = (tl >> 3) * 16, n0 = (tl & 7) * 8;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_16x8(acc, SMat{Qs, L, 1}, m0, SMat{Ks, 1, L}, n0, 0, D);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int r = acc_row(m0, e), c = acc_col(n0, e);
+      P[r * LP + c] = (c <= r && r < len) ? expf(G[r] - G[c]) * acc[e] : 0.f;
     }
-    P[i * 65 + j] = pv;
   }
   __syncthreads();
+  // dV'_intra = scale P^T dO (this block's 64 value columns)
   float *out = reinterpret_cast<float *>(dvp.p);
-  for (int idx = tid; idx < 64 * 64; idx += blockDim.x) {
-    const int j = idx / 64, c = idx % 64;
-    if (j >= len) continue;
-    float acc = 0.f;
-    for (int i = j; i < len; ++i) acc += P[i * 65 + j] * Ds[i * 65 + c];
-    out[(t0 + j) * dvp.st + h * dvp.sh + cb + c] = scale * acc;
+  for (int tl = warp * 4; tl < warp * 4 + 4; ++tl) {
+    const int m0 = (tl >> 3) * 16, n0 = (tl & 7) * 8;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_16x8(acc, SMat{P, 1, LP}, m0, SMat{Ds, LP, 1}, n0, 0, 64);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int r = acc_row(m0, e), c = acc_col(n0, e);
+      if (r < len) out[(t0 + r) * dvp.st + h * dvp.sh + cb + c] = scale * acc[e];
+    }
   }
 }
 
@@ -101,28 +98,28 @@ constexpr int kScanCols = 32;
 
 template <int D>
 struct BwdScanSmem {
-  static constexpr int kLd = D + 1;
+  static constexpr int kLdK = ld_rows(D), kLdQ = ld_cols(D), kLdC = ld_cols(kScanCols);
   static constexpr size_t bytes =
-      sizeof(float) * (D * 33 + 3 * 64 * kLd + 2 * 64 * 33 + 3 * 64);
+      sizeof(float) * (D * kLdC + 64 * kLdK + 2 * 64 * kLdQ + 2 * 64 * kLdC + 3 * 64);
 };
 
 template <int D>
 __global__ void __launch_bounds__(128)
     k_bwd_scan(int32_t H, int32_t group, View q, View k, View w, View dout, View gcum,
                float scale, const float *dht, View dvp, float *dh, float *dh0,
-               const SegInfo *__restrict__ seg) {
+               const SegInfo *__restrict__ seg, bool vec) {
   extern __shared__ float sm[];
-  constexpr int L = BwdScanSmem<D>::kLd;
+  constexpr int LK = BwdScanSmem<D>::kLdK, LQ = BwdScanSmem<D>::kLdQ, LC = BwdScanSmem<D>::kLdC;
   const int n = blockIdx.x, h = blockIdx.y, jb = blockIdx.z * kScanCols, tid = threadIdx.x;
   const int hk = h / group;
   const SegInfo si = seg[n];
-  float *dS = sm, *Ks = dS + D * 33, *Ws = Ks + 64 * L, *Qs = Ws + 64 * L, *Dos = Qs + 64 * L;
-  float *Vd = Dos + 64 * 33, *G = Vd + 64 * 33, *Dec = G + 64, *EG = Dec + 64;
+  float *dS = sm, *Ks = dS + D * LC, *Ws = Ks + 64 * LK, *Qs = Ws + 64 * LQ, *Dos = Qs + 64 * LQ;
+  float *Vd = Dos + 64 * LC, *G = Vd + 64 * LC, *Dec = G + 64, *EG = Dec + 64;
   const int64_t sbase = ((int64_t)n * H + h) * D * D;
   float *dvt = reinterpret_cast<float *>(dvp.p);
   for (int idx = tid; idx < D * kScanCols; idx += blockDim.x) {
     const int d = idx / kScanCols, j = idx % kScanCols;
-    dS[d * 33 + j] = dht ? dht[sbase + (int64_t)d * D + jb + j] : 0.f;
+    dS[d * LC + j] = dht ? dht[sbase + (int64_t)d * D + jb + j] : 0.f;
   }
   for (int c = si.n_chunks - 1; c >= 0; --c) {
     const int64_t cid = si.chunk_off + c;
@@ -132,30 +129,14 @@ __global__ void __launch_bounds__(128)
     float *dhc = dh + (cid * H + h) * D * D;
     for (int idx = tid; idx < D * kScanCols; idx += blockDim.x) {
       const int d = idx / kScanCols, j = idx % kScanCols;
-      dhc[(int64_t)d * D + jb + j] = dS[d * 33 + j];
+      dhc[(int64_t)d * D + jb + j] = dS[d * LC + j];
     }
-    for (int idx = tid; idx < 64 * D; idx += blockDim.x) {
-      const int i = idx / D, d = idx % D;
-      float kv = 0.f, wv = 0.f, qv = 0.f;
-      if (i < len) {
-        kv = ldbf(k.p, (t0 + i) * k.st + hk * k.sh + d);
-        wv = ldbf(w.p, (t0 + i) * w.st + h * w.sh + d);
-        qv = ldbf(q.p, (t0 + i) * q.st + hk * q.sh + d);
-      }
-      Ks[i * L + d] = kv;
-      Ws[i * L + d] = wv;
-      Qs[i * L + d] = qv;
-    }
-    for (int idx = tid; idx < 64 * kScanCols; idx += blockDim.x) {
-      const int i = idx / kScanCols, j = idx % kScanCols;
-      float dov = 0.f, vd = 0.f;
-      if (i < len) {
-        dov = ldbf(dout.p, (t0 + i) * dout.st + h * dout.sh + jb + j);
-        vd = dvt[(t0 + i) * dvp.st + h * dvp.sh + jb + j];
-      }
-      Dos[i * 33 + j] = dov;
-      Vd[i * 33 + j] = vd;
-    }
+    tile_bf16<64, D, 128>(Ks, LK, bf_row(k, t0, hk), k.st, len, vec);
+    tile_bf16<64, D, 128>(Ws, LQ, bf_row(w, t0, h), w.st, len, true);
+    tile_bf16<64, D, 128>(Qs, LQ, bf_row(q, t0, hk), q.st, len, vec);
+    tile_bf16<64, kScanCols, 128>(Dos, LC, bf_row(dout, t0, h) + jb,
+                                  dout.st, len, vec);
+    tile_f32<64, kScanCols, 128>(Vd, LC, dvt + t0 * dvp.st + h * dvp.sh + jb, dvp.st, len);
     if (tid < 64) G[tid] = tid < len ? ldf(gcum.p, (t0 + tid) * gcum.st + h * gcum.sh) : 0.f;
     __syncthreads();
     const float glast = G[len - 1];
@@ -164,35 +145,44 @@ __global__ void __launch_bounds__(128)
       EG[tid] = tid < len ? expf(G[tid]) : 0.f;
     }
     __syncthreads();
-    // dV' = dV'_intra + diag(e^{G_C - G}) K dS_C
-    for (int idx = tid; idx < 64 * kScanCols; idx += blockDim.x) {
-      const int i = idx / kScanCols, j = idx % kScanCols;
-      if (i >= len) continue;
-      float acc = 0.f;
-#pragma unroll 8
-      for (int d = 0; d < D; ++d) acc += Ks[i * L + d] * dS[d * 33 + j];
-      const float r = Vd[i * 33 + j] + Dec[i] * acc;
-      Vd[i * 33 + j] = r;
-      dvt[(t0 + i) * dvp.st + h * dvp.sh + jb + j] = r;
+    for (int idx = tid; idx < 64 * kScanCols; idx += blockDim.x)  // dO <- diag(e^G) dO
+      Dos[(idx / kScanCols) * LC + idx % kScanCols] *= EG[idx / kScanCols];
+    const int warp = tid >> 5;
+    // dV' = dV'_intra + diag(e^{G_C - G}) K dS_C: 16 tiles, four per warp
+    for (int tl = warp * 4; tl < warp * 4 + 4; ++tl) {
+      const int m0 = (tl >> 2) * 16, n0 = (tl & 3) * 8;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_16x8(acc, SMat{Ks, LK, 1}, m0, SMat{dS, LC, 1}, n0, 0, D);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = acc_row(m0, e), j = acc_col(n0, e);
+        if (i < len) {
+          const float r = Vd[i * LC + j] + Dec[i] * acc[e];
+          Vd[i * LC + j] = r;
+          dvt[(t0 + i) * dvp.st + h * dvp.sh + jb + j] = r;
+        }
+      }
     }
     __syncthreads();
-    // dS_0 = e^{G_C} dS_C + scale Q^T diag(e^G) dO - W^T dV'
+    // dS_0 = e^{G_C} dS_C + scale Q^T diag(e^G) dO - W^T dV': D/16 x 4 tiles over 4 warps
     const float eg = expf(glast);
-    for (int idx = tid; idx < D * kScanCols; idx += blockDim.x) {
-      const int d = idx / kScanCols, j = idx % kScanCols;
-      float inj = 0.f, corr = 0.f;
-      for (int i = 0; i < len; ++i) {
-        inj += Qs[i * L + d] * EG[i] * Dos[i * 33 + j];
-        corr += Ws[i * L + d] * Vd[i * 33 + j];
+    for (int tl = warp; tl < (D / 16) * 4; tl += 4) {
+      const int m0 = (tl >> 2) * 16, n0 = (tl & 3) * 8;
+      float inj[4] = {0.f, 0.f, 0.f, 0.f}, corr[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_16x8(inj, SMat{Qs, 1, LQ}, m0, SMat{Dos, LC, 1}, n0, 0, 64);
+      mma_16x8(corr, SMat{Ws, 1, LQ}, m0, SMat{Vd, LC, 1}, n0, 0, 64);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int d = acc_row(m0, e), j = acc_col(n0, e);
+        dS[d * LC + j] = eg * dS[d * LC + j] + scale * inj[e] - corr[e];
       }
-      dS[d * 33 + j] = eg * dS[d * 33 + j] + scale * inj - corr;
     }
   }
   if (dh0) {
     __syncthreads();
     for (int idx = tid; idx < D * kScanCols; idx += blockDim.x) {
       const int d = idx / kScanCols, j = idx % kScanCols;
-      dh0[sbase + (int64_t)d * D + jb + j] = dS[d * 33 + j];
+      dh0[sbase + (int64_t)d * D + jb + j] = dS[d * LC + j];
     }
   }
 }
@@ -202,7 +192,7 @@ constexpr int kSRows = 32;  // key rows of S_0 / dS_C per block
 
 template <int D>
 struct SgradSmem {
-  static constexpr int kLd = D + 1;
+  static constexpr int kLd = ld_rows(D);
   static constexpr size_t bytes =
       sizeof(float) * (2 * kSRows * kLd + 3 * 64 * kLd + 2 * 64 + 256);
 };
@@ -212,7 +202,7 @@ __global__ void __launch_bounds__(256)
     k_bwd_sgrad(View dout, View v_new, View gcum, float scale, const __nv_bfloat16 *hbuf,
                 const float *dh, View dvp, View dqh, View dkh, View dw, float *sdot,
                 const ChunkInfo *__restrict__ chunks, const int32_t *__restrict__ n_chunks,
-                int32_t H) {
+                int32_t H, bool vec) {
   extern __shared__ float sm[];
   constexpr int L = SgradSmem<D>::kLd;
   const int cid = blockIdx.x, h = blockIdx.y, rb = blockIdx.z * kSRows, tid = threadIdx.x;
@@ -224,24 +214,13 @@ __global__ void __launch_bounds__(256)
   float *dV = Vp + 64 * L, *Dec = dV + 64 * L, *EG = Dec + 64, *red = EG + 64;
   const __nv_bfloat16 *hc = hbuf + ((int64_t)cid * H + h) * D * D;
   const float *dhc = dh + ((int64_t)cid * H + h) * D * D;
-  for (int idx = tid; idx < kSRows * D; idx += blockDim.x) {
-    const int r = idx / D, j = idx % D;
-    S0[r * L + j] = __bfloat162float(hc[(int64_t)(rb + r) * D + j]);
-    dS[r * L + j] = dhc[(int64_t)(rb + r) * D + j];
-  }
+  tile_bf16<kSRows, D, 256>(S0, L, hc + (int64_t)rb * D, D, kSRows, true);
+  tile_f32<kSRows, D, 256>(dS, L, dhc + (int64_t)rb * D, D, kSRows);
   const float *dvt = reinterpret_cast<const float *>(dvp.p);
-  for (int idx = tid; idx < 64 * D; idx += blockDim.x) {
-    const int i = idx / D, j = idx % D;
-    float a = 0.f, b = 0.f, c = 0.f;
-    if (i < len) {
-      a = ldbf(dout.p, (t0 + i) * dout.st + h * dout.sh + j);
-      b = ldbf(v_new.p, (t0 + i) * v_new.st + h * v_new.sh + j);
-      c = dvt[(t0 + i) * dvp.st + h * dvp.sh + j];
-    }
-    Dos[i * L + j] = a;
-    Vp[i * L + j] = b;
-    dV[i * L + j] = c;
-  }
+  tile_bf16<64, D, 256>(Dos, L, bf_row(dout, t0, h), dout.st, len, vec);
+  tile_bf16<64, D, 256>(Vp, L, bf_row(v_new, t0, h), v_new.st, len,
+                        true);
+  tile_f32<64, D, 256>(dV, L, dvt + t0 * dvp.st + h * dvp.sh, dvp.st, len);
   if (tid < 64) {
     const float gi = tid < len ? ldf(gcum.p, (t0 + tid) * gcum.st + h * gcum.sh) : 0.f;
     const float gl = ldf(gcum.p, (t0 + len - 1) * gcum.st + h * gcum.sh);
@@ -251,19 +230,23 @@ __global__ void __launch_bounds__(256)
   __syncthreads();
   float *q_out = reinterpret_cast<float *>(dqh.p), *k_out = reinterpret_cast<float *>(dkh.p);
   float *w_out = reinterpret_cast<float *>(dw.p);
-  for (int idx = tid; idx < 64 * kSRows; idx += blockDim.x) {
-    const int i = idx / kSRows, r = idx % kSRows;
-    if (i >= len) continue;
-    float aq = 0.f, ak = 0.f, aw = 0.f;
-#pragma unroll 4
-    for (int j = 0; j < D; ++j) {
-      aq += Dos[i * L + j] * S0[r * L + j];
-      ak += Vp[i * L + j] * dS[r * L + j];
-      aw += dV[i * L + j] * S0[r * L + j];
+  // 64 x 32 outputs of each product: 16 tiles, two per warp
+  const int warp = tid >> 5;
+  for (int tl = warp * 2; tl < warp * 2 + 2; ++tl) {
+    const int m0 = (tl >> 2) * 16, n0 = (tl & 3) * 8;
+    float aq[4] = {0.f, 0.f, 0.f, 0.f}, ak[4] = {0.f, 0.f, 0.f, 0.f}, aw[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_16x8(aq, SMat{Dos, L, 1}, m0, SMat{S0, 1, L}, n0, 0, D);
+    mma_16x8(ak, SMat{Vp, L, 1}, m0, SMat{dS, 1, L}, n0, 0, D);
+    mma_16x8(aw, SMat{dV, L, 1}, m0, SMat{S0, 1, L}, n0, 0, D);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = acc_row(m0, e), r = acc_col(n0, e);
+      if (i < len) {
+        q_out[(t0 + i) * dqh.st + h * dqh.sh + rb + r] = scale * EG[i] * aq[e];
+        k_out[(t0 + i) * dkh.st + h * dkh.sh + rb + r] = Dec[i] * ak[e];
+        w_out[(t0 + i) * dw.st + h * dw.sh + rb + r] = -aw[e];
+      }
     }
-    q_out[(t0 + i) * dqh.st + h * dqh.sh + rb + r] = scale * EG[i] * aq;
-    k_out[(t0 + i) * dkh.st + h * dkh.sh + rb + r] = Dec[i] * ak;
-    w_out[(t0 + i) * dw.st + h * dw.sh + rb + r] = -aw;
   }
   // <dS_C, S_0> over this block's key rows (fixed-order tree reduction)
   float part = 0.f;
@@ -283,104 +266,117 @@ __global__ void __launch_bounds__(256)
 // ---------------------------------------------------------------- intra-chunk terms
 template <int D>
 struct IntraSmem {
-  static constexpr int kLd = D + 1;
-  static constexpr size_t bytes = sizeof(float) * (4 * 64 * kLd + 2 * 64 * 65 + 5 * 64);
+  static constexpr int kLd = ld_rows(D), kLdE = ld_rows(64);
+  static constexpr size_t bytes = sizeof(float) * (4 * 64 * kLd + 2 * 64 * kLdE + 7 * 64);
 };
 
-// Threads cover a 64 x D tile as (row i = tid / 4, columns tid % 4 + 4 m): the four
-// threads of a row are neighbouring lanes, so row sums are two shuffles.
+// Warp w owns rows 16 (w % 4) .. +16 and half of the D columns (w / 4) of the 64 x D
+// products; row sums go through a shuffle inside the tile, then two per-warp partials
+// added in a fixed order.
 template <int D>
 __global__ void __launch_bounds__(256)
     k_bwd_intra(int32_t group, View q, View k, View dout, View v_new, View gcum, float scale,
                 View dqh, View dkh, float *dga, const ChunkInfo *__restrict__ chunks,
-                const int32_t *__restrict__ n_chunks, int32_t H) {
+                const int32_t *__restrict__ n_chunks, int32_t H, bool vec) {
   extern __shared__ float sm[];
-  constexpr int L = IntraSmem<D>::kLd;
+  constexpr int L = IntraSmem<D>::kLd, LE = IntraSmem<D>::kLdE;
   const int cid = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   if (cid >= *n_chunks) return;
   const ChunkInfo ci = chunks[cid];
   const int len = ci.len, hk = h / group;
   const int64_t t0 = ci.start;
   float *Qs = sm, *Ks = Qs + 64 * L, *Dos = Ks + 64 * L, *Vp = Dos + 64 * L;
-  float *E = Vp + 64 * L, *R = E + 64 * 65, *G = R + 64 * 65, *rowR = G + 64, *colR = rowR + 64;
-  float *aS = colR + 64, *cS = aS + 64;
-  for (int idx = tid; idx < 64 * D; idx += blockDim.x) {
-    const int i = idx / D, d = idx % D;
-    float a = 0.f, b = 0.f, c = 0.f, e = 0.f;
-    if (i < len) {
-      a = ldbf(q.p, (t0 + i) * q.st + hk * q.sh + d);
-      b = ldbf(k.p, (t0 + i) * k.st + hk * k.sh + d);
-      c = ldbf(dout.p, (t0 + i) * dout.st + h * dout.sh + d);
-      e = ldbf(v_new.p, (t0 + i) * v_new.st + h * v_new.sh + d);
-    }
-    Qs[i * L + d] = a;
-    Ks[i * L + d] = b;
-    Dos[i * L + d] = c;
-    Vp[i * L + d] = e;
-  }
+  float *E = Vp + 64 * L, *R = E + 64 * LE, *G = R + 64 * LE, *rowR = G + 64, *colR = rowR + 64;
+  float *aP = colR + 64, *cP = aP + 128;  // [2][64] partial row sums
+  tile_bf16<64, D, 256>(Qs, L, bf_row(q, t0, hk), q.st, len, vec);
+  tile_bf16<64, D, 256>(Ks, L, bf_row(k, t0, hk), k.st, len, vec);
+  tile_bf16<64, D, 256>(Dos, L, bf_row(dout, t0, h), dout.st, len, vec);
+  tile_bf16<64, D, 256>(Vp, L, bf_row(v_new, t0, h), v_new.st, len,
+                        true);
   if (tid < 64) G[tid] = tid < len ? ldf(gcum.p, (t0 + tid) * gcum.st + h * gcum.sh) : 0.f;
+  const int warp = tid >> 5;
+  // this thread's elements of the dQ / dK accumulators (written by k_bwd_sgrad), loaded
+  // now so that the loads overlap the products below
+  float *q_out = reinterpret_cast<float *>(dqh.p), *k_out = reinterpret_cast<float *>(dkh.p);
+  const int m0 = (warp & 3) * 16, half = warp >> 2;
+  constexpr int kCT = D / 16;  // column tiles per warp
+  float qpre[kCT][4], kpre[kCT][4];
+#pragma unroll
+  for (int c = 0; c < kCT; ++c)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = acc_row(m0, e), d = acc_col((half * kCT + c) * 8, e);
+      qpre[c][e] = i < len ? q_out[(t0 + i) * dqh.st + h * dqh.sh + d] : 0.f;
+      kpre[c][e] = i < len ? k_out[(t0 + i) * dkh.st + h * dkh.sh + d] : 0.f;
+    }
   __syncthreads();
   // E_ij = scale (do_i . v'_j) Gam_ij and R_ij = E_ij (q_i . k_j), j <= i
-  for (int idx = tid; idx < 64 * 64; idx += blockDim.x) {
-    const int i = idx / 64, j = idx % 64;
-    float e = 0.f, r = 0.f;
-    if (j <= i && i < len) {
-      float dv = 0.f, qk = 0.f;
-#pragma unroll 8
-      for (int d = 0; d < D; ++d) {
-        dv += Dos[i * L + d] * Vp[j * L + d];
-        qk += Qs[i * L + d] * Ks[j * L + d];
-      }
-      e = scale * dv * expf(G[i] - G[j]);
-      r = e * qk;
+  for (int tl = warp * 4; tl < warp * 4 + 4; ++tl) {
+    const int m0 = (tl >> 3) * 16, n0 = (tl & 7) * 8;
+    float dv[4] = {0.f, 0.f, 0.f, 0.f}, qk[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_16x8(dv, SMat{Dos, L, 1}, m0, SMat{Vp, 1, L}, n0, 0, D);
+    mma_16x8(qk, SMat{Qs, L, 1}, m0, SMat{Ks, 1, L}, n0, 0, D);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = acc_row(m0, e), j = acc_col(n0, e);
+      const float ev = (j <= i && i < len) ? scale * dv[e] * expf(G[i] - G[j]) : 0.f;
+      E[i * LE + j] = ev;
+      R[i * LE + j] = ev * qk[e];
     }
-    E[i * 65 + j] = e;
-    R[i * 65 + j] = r;
   }
   __syncthreads();
   if (tid < 64) {
     float s = 0.f;
-    for (int j = 0; j < 64; ++j) s += R[tid * 65 + j];
+    for (int j = 0; j < 64; ++j) s += R[tid * LE + j];
     rowR[tid] = s;
   } else if (tid < 128) {
     const int j = tid - 64;
     float s = 0.f;
-    for (int i = 0; i < 64; ++i) s += R[i * 65 + j];
+    for (int i = 0; i < 64; ++i) s += R[i * LE + j];
     colR[j] = s;
   }
-  const int i = tid >> 2, sub = tid & 3;
-  float apart = 0.f, cpart = 0.f;
-  float *q_out = reinterpret_cast<float *>(dqh.p), *k_out = reinterpret_cast<float *>(dkh.p);
-  if (i < len) {
-    for (int d = sub; d < D; d += 4) {
-      float dq = 0.f, dk = 0.f;
-      for (int j = 0; j <= i; ++j) dq += E[i * 65 + j] * Ks[j * L + d];
-      for (int a = i; a < len; ++a) dk += E[a * 65 + i] * Qs[a * L + d];
-      const int64_t oq = (t0 + i) * dqh.st + h * dqh.sh + d;
-      const int64_t ok = (t0 + i) * dkh.st + h * dkh.sh + d;
-      const float q_inter = q_out[oq], k_state = k_out[ok];
-      apart += Qs[i * L + d] * q_inter;
-      cpart += Ks[i * L + d] * k_state;
-      q_out[oq] = q_inter + dq;
-      k_out[ok] = k_state + dk;
+  // dQ += E K, dK += E^T Q; a_i = q_i . dQ_inter_i and c_i = k_i . dK_state_i on the way
+  float ap[2] = {0.f, 0.f}, cp[2] = {0.f, 0.f};
+#pragma unroll
+  for (int c = 0; c < kCT; ++c) {
+    const int n0 = (half * kCT + c) * 8;
+    float dq[4] = {0.f, 0.f, 0.f, 0.f}, dk[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_16x8(dq, SMat{E, LE, 1}, m0, SMat{Ks, L, 1}, n0, 0, 64);
+    mma_16x8(dk, SMat{E, 1, LE}, m0, SMat{Qs, L, 1}, n0, 0, 64);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = acc_row(m0, e), d = acc_col(n0, e);
+      if (i < len) {
+        ap[e >> 1] += Qs[i * L + d] * qpre[c][e];
+        cp[e >> 1] += Ks[i * L + d] * kpre[c][e];
+        q_out[(t0 + i) * dqh.st + h * dqh.sh + d] = qpre[c][e] + dq[e];
+        k_out[(t0 + i) * dkh.st + h * dkh.sh + d] = kpre[c][e] + dk[e];
+      }
     }
   }
-  apart += __shfl_xor_sync(0xffffffffu, apart, 1);
-  apart += __shfl_xor_sync(0xffffffffu, apart, 2);
-  cpart += __shfl_xor_sync(0xffffffffu, cpart, 1);
-  cpart += __shfl_xor_sync(0xffffffffu, cpart, 2);
-  if (sub == 0) {
-    aS[i] = apart;
-    cS[i] = cpart;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    ap[r] += __shfl_xor_sync(0xffffffffu, ap[r], 1);
+    ap[r] += __shfl_xor_sync(0xffffffffu, ap[r], 2);
+    cp[r] += __shfl_xor_sync(0xffffffffu, cp[r], 1);
+    cp[r] += __shfl_xor_sync(0xffffffffu, cp[r], 2);
+  }
+  if ((tid & 3) == 0) {
+    const int r0 = m0 + ((tid & 31) >> 2);
+    aP[half * 64 + r0] = ap[0];
+    aP[half * 64 + r0 + 8] = ap[1];
+    cP[half * 64 + r0] = cp[0];
+    cP[half * 64 + r0 + 8] = cp[1];
   }
   __syncthreads();
   // dG from the output (e^G on S_0, Gam) and from the state's e^{G_C - G_i} factors;
   // the e^{G_C} S_0 term is added by k_bwd_wy
   if (tid < len) {
-    float v = aS[tid] - cS[tid] + rowR[tid] - colR[tid];
+    const float c_t = cP[tid] + cP[64 + tid];
+    float v = (aP[tid] + aP[64 + tid]) - c_t + rowR[tid] - colR[tid];
     if (tid == len - 1) {
       float sc = 0.f;
-      for (int r = 0; r < len; ++r) sc += cS[r];
+      for (int r = 0; r < len; ++r) sc += cP[r] + cP[64 + r];
       v += sc;
     }
     dga[(t0 + tid) * H + h] = v;
@@ -390,8 +386,9 @@ __global__ void __launch_bounds__(256)
 // ---------------------------------------------------------------- WY / solve backward
 template <int D>
 struct WySmem {
-  static constexpr int kLd = D + 1;
-  static constexpr size_t bytes = sizeof(float) * (4 * 64 * kLd + 4 * 64 * 65 + 8 * 64);
+  static constexpr int kLd = ld_rows(D), kLdK = ld_rows(64), kLdT = ld_cols(64);
+  static constexpr size_t bytes =
+      sizeof(float) * (4 * 64 * kLd + 64 * kLdK + 3 * 64 * kLdT + 11 * 64);
 };
 
 template <int D>
@@ -399,134 +396,135 @@ __global__ void __launch_bounds__(256)
     k_bwd_wy(int32_t group, View k, View v, View beta, View gcum, View dvp, View dw, View dkh,
              const float *dga, const float *sdot, View dv_out, View dbeta_out, View dg_out,
              const ChunkInfo *__restrict__ chunks, const int32_t *__restrict__ n_chunks,
-             int32_t H) {
+             int32_t H, bool vec) {
   extern __shared__ float sm[];
-  constexpr int L = WySmem<D>::kLd;
+  constexpr int L = WySmem<D>::kLd, LK = WySmem<D>::kLdK, LT = WySmem<D>::kLdT;
   const int cid = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   if (cid >= *n_chunks) return;
   const ChunkInfo ci = chunks[cid];
   const int len = ci.len, hk = h / group;
   const int64_t t0 = ci.start;
   float *Ks = sm, *Vs = Ks + 64 * L, *dVs = Vs + 64 * L, *dWs = dVs + 64 * L;
-  float *KK = dWs + 64 * L, *Tm = KK + 64 * 65, *dT = Tm + 64 * 65, *X = dT + 64 * 65;
-  float *G = X + 64 * 65, *B = G + 64, *BG = B + 64, *EGv = BG + 64, *dGt = EGv + 64;
-  float *dbS = dGt + 64, *dgbS = dbS + 64;
+  float *KK = dWs + 64 * L, *Tm = KK + 64 * LK, *dT = Tm + 64 * LT, *X = dT + 64 * LT;
+  float *G = X + 64 * LT, *B = G + 64, *BG = B + 64, *EGv = BG + 64, *dGt = EGv + 64;
+  float *baP = dGt + 64, *bbP = baP + 128;  // [2][64] partial row sums
   const float *dvt = reinterpret_cast<const float *>(dvp.p), *dwt = reinterpret_cast<const float *>(dw.p);
-  for (int idx = tid; idx < 64 * D; idx += blockDim.x) {
-    const int i = idx / D, d = idx % D;
-    float a = 0.f, b = 0.f, c = 0.f, e = 0.f;
-    if (i < len) {
-      a = ldbf(k.p, (t0 + i) * k.st + hk * k.sh + d);
-      b = ldbf(v.p, (t0 + i) * v.st + h * v.sh + d);
-      c = dvt[(t0 + i) * dvp.st + h * dvp.sh + d];
-      e = dwt[(t0 + i) * dw.st + h * dw.sh + d];
-    }
-    Ks[i * L + d] = a;
-    Vs[i * L + d] = b;
-    dVs[i * L + d] = c;
-    dWs[i * L + d] = e;
-  }
+  tile_bf16<64, D, 256>(Ks, L, bf_row(k, t0, hk), k.st, len, vec);
+  tile_bf16<64, D, 256>(Vs, L, bf_row(v, t0, h), v.st, len, vec);
+  tile_f32<64, D, 256>(dVs, L, dvt + t0 * dvp.st + h * dvp.sh, dvp.st, len);
+  tile_f32<64, D, 256>(dWs, L, dwt + t0 * dw.st + h * dw.sh, dw.st, len);
   if (tid < 64) {
     const bool in = tid < len;
     G[tid] = in ? ldf(gcum.p, (t0 + tid) * gcum.st + h * gcum.sh) : 0.f;
     B[tid] = in ? ldbf(beta.p, (t0 + tid) * beta.st + h * beta.sh) : 0.f;
   }
+  const int warp = tid >> 5;
+  // this thread's elements of the dK accumulator, loaded early (used at the end)
+  float *dvo = reinterpret_cast<float *>(dv_out.p), *dko = reinterpret_cast<float *>(dkh.p);
+  const int m0 = (warp & 3) * 16, half = warp >> 2;
+  constexpr int kCT = D / 16;
+  float kpre[kCT][4];
+#pragma unroll
+  for (int c = 0; c < kCT; ++c)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j = acc_row(m0, e), d = acc_col((half * kCT + c) * 8, e);
+      kpre[c][e] = j < len ? dko[(t0 + j) * dkh.st + h * dkh.sh + d] : 0.f;
+    }
   __syncthreads();
   if (tid < 64) {
     EGv[tid] = tid < len ? expf(G[tid]) : 0.f;
     BG[tid] = B[tid] * EGv[tid];
   }
-  // raw key products k_i . k_j, j < i
-  for (int idx = tid; idx < 64 * 64; idx += blockDim.x) {
-    const int i = idx / 64, j = idx % 64;
-    float dot = 0.f;
-    if (j < i && i < len) {
-#pragma unroll 8
-      for (int d = 0; d < D; ++d) dot += Ks[i * L + d] * Ks[j * L + d];
+  // raw key products k_i . k_j (j < i) and A_ij = beta_i Gam_ij k_i . k_j
+  for (int tl = warp * 4; tl < warp * 4 + 4; ++tl) {
+    const int m0 = (tl >> 3) * 16, n0 = (tl & 7) * 8;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_16x8(acc, SMat{Ks, L, 1}, m0, SMat{Ks, 1, L}, n0, 0, D);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = acc_row(m0, e), j = acc_col(n0, e);
+      const bool lo = j < i && i < len;
+      KK[i * LK + j] = lo ? acc[e] : 0.f;
+      X[i * LT + j] = lo ? B[i] * expf(G[i] - G[j]) * acc[e] : 0.f;
     }
-    KK[i * 65 + j] = dot;
-    X[i * 65 + j] = (j < i && i < len) ? B[i] * expf(G[i] - G[j]) * dot : 0.f;  // A_ij
   }
   __syncthreads();
-  if (tid < 64) {  // column c of T = (I + A)^-1, A_ij = beta_i Gam_ij k_i.k_j
-    const int c = tid;
-    for (int i = 0; i < 64; ++i) {
-      float x = (i == c) ? 1.f : 0.f;
-      for (int j = c; j < i; ++j) x -= X[i * 65 + j] * Tm[j * 65 + c];
-      Tm[i * 65 + c] = x;
+  solve_unit_lower64(X, LT, Tm, LT, dT);  // T = (I + A)^-1; dT's space as scratch until it is formed
+  // dT_ij = beta_j (dU_i . v_j) + beta_j e^{G_j} (dW_i . k_j), i > j (the only part dA needs)
+  for (int tl = warp * 4; tl < warp * 4 + 4; ++tl) {
+    const int m0 = (tl >> 3) * 16, n0 = (tl & 7) * 8;
+    float du[4] = {0.f, 0.f, 0.f, 0.f}, dwk[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_16x8(du, SMat{dVs, L, 1}, m0, SMat{Vs, 1, L}, n0, 0, D);
+    mma_16x8(dwk, SMat{dWs, L, 1}, m0, SMat{Ks, 1, L}, n0, 0, D);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = acc_row(m0, e), j = acc_col(n0, e);
+      dT[i * LT + j] = (j < i && i < len) ? B[j] * du[e] + BG[j] * dwk[e] : 0.f;
     }
   }
-  // dT_ij = dU_i . (beta_j v_j) + dW_i . (beta_j e^{G_j} k_j), i > j (the only part dA needs)
+  __syncthreads();
+  // X = dT T^T
+  for (int tl = warp * 4; tl < warp * 4 + 4; ++tl) {
+    const int m0 = (tl >> 3) * 16, n0 = (tl & 7) * 8;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_16x8(acc, SMat{dT, LT, 1}, m0, SMat{Tm, 1, LT}, n0, 0, 64);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) X[acc_row(m0, e) * LT + acc_col(n0, e)] = acc[e];
+  }
+  __syncthreads();
+  // dA = -T^T X (i > j) into dT's place
+  for (int tl = warp * 4; tl < warp * 4 + 4; ++tl) {
+    const int m0 = (tl >> 3) * 16, n0 = (tl & 7) * 8;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_16x8(acc, SMat{Tm, 1, LT}, m0, SMat{X, LT, 1}, n0, 0, 64);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = acc_row(m0, e), j = acc_col(n0, e);
+      dT[i * LT + j] = (j < i && i < len) ? -acc[e] : 0.f;
+    }
+  }
+  __syncthreads();
+  // X <- B_ij = dA_ij beta_i Gam_ij (i > j)
   for (int idx = tid; idx < 64 * 64; idx += blockDim.x) {
     const int i = idx / 64, j = idx % 64;
-    float acc = 0.f;
-    if (j < i && i < len) {
-      float du = 0.f, dwk = 0.f;
-#pragma unroll 8
-      for (int d = 0; d < D; ++d) {
-        du += dVs[i * L + d] * Vs[j * L + d];
-        dwk += dWs[i * L + d] * Ks[j * L + d];
+    X[i * LT + j] = (j < i && i < len) ? dT[i * LT + j] * B[i] * expf(G[i] - G[j]) : 0.f;
+  }
+  __syncthreads();
+  // per row j: T^T dU, T^T dW, (B + B^T) K; warp w owns rows 16 (w % 4) .. +16, half the columns
+  float ba[2] = {0.f, 0.f}, bb[2] = {0.f, 0.f};
+#pragma unroll
+  for (int c = 0; c < kCT; ++c) {
+    const int n0 = (half * kCT + c) * 8;
+    float tdu[4] = {0.f, 0.f, 0.f, 0.f}, tdw[4] = {0.f, 0.f, 0.f, 0.f}, kc[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_16x8(tdu, SMat{Tm, 1, LT}, m0, SMat{dVs, L, 1}, n0, 0, 64);
+    mma_16x8(tdw, SMat{Tm, 1, LT}, m0, SMat{dWs, L, 1}, n0, 0, 64);
+    mma_16x8(kc, SMat{X, LT, 1}, m0, SMat{Ks, L, 1}, n0, 0, 64);
+    mma_16x8(kc, SMat{X, 1, LT}, m0, SMat{Ks, L, 1}, n0, 0, 64);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j = acc_row(m0, e), d = acc_col(n0, e);
+      if (j < len) {
+        dvo[(t0 + j) * dv_out.st + h * dv_out.sh + d] = B[j] * tdu[e];
+        ba[e >> 1] += Vs[j * L + d] * tdu[e];
+        bb[e >> 1] += Ks[j * L + d] * tdw[e];
+        dko[(t0 + j) * dkh.st + h * dkh.sh + d] = kpre[c][e] + BG[j] * tdw[e] + kc[e];
       }
-      acc = B[j] * du + BG[j] * dwk;
-    }
-    dT[i * 65 + j] = acc;
-  }
-  __syncthreads();
-  // X = dT T^T:  X_ab = sum_{c} dT_ac T_bc  (c < a, c <= b)
-  for (int idx = tid; idx < 64 * 64; idx += blockDim.x) {
-    const int a = idx / 64, b = idx % 64;
-    float acc = 0.f;
-    const int cmax = min(a, b + 1);
-    for (int c = 0; c < cmax; ++c) acc += dT[a * 65 + c] * Tm[b * 65 + c];
-    X[a * 65 + b] = acc;
-  }
-  __syncthreads();
-  // dA = -T^T X, i > j:  dA_ij = -sum_{a >= i} T_ai X_aj; then Q_ij = dA_ij A_ij into X's
-  // place is not needed: dA goes to dT (dT is dead once X is formed)
-  for (int idx = tid; idx < 64 * 64; idx += blockDim.x) {
-    const int i = idx / 64, j = idx % 64;
-    float acc = 0.f;
-    if (j < i && i < len) {
-      for (int a = i; a < len; ++a) acc += Tm[a * 65 + i] * X[a * 65 + j];
-      acc = -acc;
-    }
-    dT[i * 65 + j] = acc;
-  }
-  __syncthreads();
-  // X <- B_ij = dA_ij beta_i Gam_ij (i > j); dbeta_c and dG_c from dA o A
-  for (int idx = tid; idx < 64 * 64; idx += blockDim.x) {
-    const int i = idx / 64, j = idx % 64;
-    X[i * 65 + j] = (j < i && i < len) ? dT[i * 65 + j] * B[i] * expf(G[i] - G[j]) : 0.f;
-  }
-  __syncthreads();
-  // per row j (tid / 4), columns tid % 4 + 4 m
-  const int j = tid >> 2, sub = tid & 3;
-  float dba = 0.f, dbb = 0.f;
-  float *dvo = reinterpret_cast<float *>(dv_out.p), *dko = reinterpret_cast<float *>(dkh.p);
-  if (j < len) {
-    for (int d = sub; d < D; d += 4) {
-      float tdu = 0.f, tdw = 0.f;
-      for (int i = j; i < len; ++i) {
-        tdu += Tm[i * 65 + j] * dVs[i * L + d];
-        tdw += Tm[i * 65 + j] * dWs[i * L + d];
-      }
-      dvo[(t0 + j) * dv_out.st + h * dv_out.sh + d] = B[j] * tdu;
-      dba += Vs[j * L + d] * tdu;
-      dbb += Ks[j * L + d] * tdw;
-      float kc = 0.f;
-      for (int x = 0; x < j; ++x) kc += X[j * 65 + x] * Ks[x * L + d];
-      for (int a = j + 1; a < len; ++a) kc += X[a * 65 + j] * Ks[a * L + d];
-      const int64_t ok = (t0 + j) * dkh.st + h * dkh.sh + d;
-      dko[ok] = dko[ok] + BG[j] * tdw + kc;
     }
   }
-  dba += __shfl_xor_sync(0xffffffffu, dba, 1);
-  dba += __shfl_xor_sync(0xffffffffu, dba, 2);
-  dbb += __shfl_xor_sync(0xffffffffu, dbb, 1);
-  dbb += __shfl_xor_sync(0xffffffffu, dbb, 2);
-  if (sub == 0) {
-    dbS[j] = dba;
-    dgbS[j] = dbb;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    ba[r] += __shfl_xor_sync(0xffffffffu, ba[r], 1);
+    ba[r] += __shfl_xor_sync(0xffffffffu, ba[r], 2);
+    bb[r] += __shfl_xor_sync(0xffffffffu, bb[r], 1);
+    bb[r] += __shfl_xor_sync(0xffffffffu, bb[r], 2);
+  }
+  if ((tid & 3) == 0) {
+    const int r0 = m0 + ((tid & 31) >> 2);
+    baP[half * 64 + r0] = ba[0];
+    baP[half * 64 + r0 + 8] = ba[1];
+    bbP[half * 64 + r0] = bb[0];
+    bbP[half * 64 + r0 + 8] = bb[1];
   }
   __syncthreads();
   if (tid < 64) {
@@ -534,14 +532,14 @@ __global__ void __launch_bounds__(256)
     float dbc = 0.f, rowq = 0.f, colq = 0.f;
     if (r < len) {
       for (int x = 0; x < r; ++x) {
-        const float gam = expf(G[r] - G[x]);
-        dbc += dT[r * 65 + x] * gam * KK[r * 65 + x];
-        rowq += X[r * 65 + x] * KK[r * 65 + x];
+        dbc += dT[r * LT + x] * expf(G[r] - G[x]) * KK[r * LK + x];
+        rowq += X[r * LT + x] * KK[r * LK + x];
       }
-      for (int a = r + 1; a < len; ++a) colq += X[a * 65 + r] * KK[a * 65 + r];
-      float* dbo = reinterpret_cast<float *>(dbeta_out.p);
-      dbo[(t0 + r) * dbeta_out.st + h * dbeta_out.sh] = dbS[r] + EGv[r] * dgbS[r] + dbc;
-      float gt = dga[(t0 + r) * H + h] + BG[r] * dgbS[r] + rowq - colq;
+      for (int a = r + 1; a < len; ++a) colq += X[a * LT + r] * KK[a * LK + r];
+      const float dba = baP[r] + baP[64 + r], dbb = bbP[r] + bbP[64 + r];
+      float *dbo = reinterpret_cast<float *>(dbeta_out.p);
+      dbo[(t0 + r) * dbeta_out.st + h * dbeta_out.sh] = dba + EGv[r] * dbb + dbc;
+      float gt = dga[(t0 + r) * H + h] + BG[r] * dbb + rowq - colq;
       if (r == len - 1) {
         float sd = 0.f;
         for (int b = 0; b < D / kSRows; ++b) sd += sdot[((int64_t)cid * H + h) * (D / kSRows) + b];
@@ -633,6 +631,11 @@ cudaError_t launch_bwd_d(const BwdArgs &a, const BwdWs &w, cudaStream_t stream) 
   const View vdvp{w.dvp, HD, D}, vdw{w.dw, HD, D};
   const View vdqh = group > 1 ? View{w.dqh, HD, D} : a.dq;
   const View vdkh = group > 1 ? View{w.dkh, HD, D} : a.dk;
+  // 16-byte vector loads of the caller's bf16 tensors when their rows allow it
+  auto al = [](const View &x) {
+    return (reinterpret_cast<uintptr_t>(x.p) & 15) == 0 && x.st % 8 == 0 && x.sh % 8 == 0;
+  };
+  const bool vec = al(a.q) && al(a.k) && al(a.v) && al(a.dout);
   cudaError_t e;
   // forward recompute: G, W, U (stage 1), chunk states h and V' (stage 2)
   if ((e = launch_prep(s, a.k, a.v, a.g, a.beta, vw, vu, vg, a.seg, a.chunks, a.n_chunks,
@@ -644,27 +647,28 @@ cudaError_t launch_bwd_d(const BwdArgs &a, const BwdWs &w, cudaStream_t stream) 
   const dim3 gc((unsigned)s.chunk_cap, (unsigned)s.H);
   if ((e = set_smem(k_bwd_dv_intra<D>, DvIntraSmem<D>::bytes)) != cudaSuccess) return e;
   k_bwd_dv_intra<D><<<dim3(gc.x, gc.y, D / 64), 256, DvIntraSmem<D>::bytes, stream>>>(
-      group, a.q, a.k, a.dout, vg, a.scale, vdvp, a.chunks, a.n_chunks);
+      group, a.q, a.k, a.dout, vg, a.scale, vdvp, a.chunks, a.n_chunks, vec);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = set_smem(k_bwd_scan<D>, BwdScanSmem<D>::bytes)) != cudaSuccess) return e;
   k_bwd_scan<D><<<dim3((unsigned)s.n_seq, (unsigned)s.H, D / kScanCols), 128,
                   BwdScanSmem<D>::bytes, stream>>>(s.H, group, a.q, a.k, vw, a.dout, vg,
-                                                   a.scale, a.dht, vdvp, w.dh, a.dh0, a.seg);
+                                                   a.scale, a.dht, vdvp, w.dh, a.dh0, a.seg,
+                                                   vec);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = set_smem(k_bwd_sgrad<D>, SgradSmem<D>::bytes)) != cudaSuccess) return e;
   k_bwd_sgrad<D><<<dim3(gc.x, gc.y, D / kSRows), 256, SgradSmem<D>::bytes, stream>>>(
       a.dout, vn, vg, a.scale, reinterpret_cast<const __nv_bfloat16 *>(w.h), w.dh, vdvp, vdqh,
-      vdkh, vdw, w.sdot, a.chunks, a.n_chunks, s.H);
+      vdkh, vdw, w.sdot, a.chunks, a.n_chunks, s.H, vec);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = set_smem(k_bwd_intra<D>, IntraSmem<D>::bytes)) != cudaSuccess) return e;
   k_bwd_intra<D><<<gc, 256, IntraSmem<D>::bytes, stream>>>(group, a.q, a.k, a.dout, vn, vg,
                                                             a.scale, vdqh, vdkh, w.dga,
-                                                            a.chunks, a.n_chunks, s.H);
+                                                            a.chunks, a.n_chunks, s.H, vec);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = set_smem(k_bwd_wy<D>, WySmem<D>::bytes)) != cudaSuccess) return e;
   k_bwd_wy<D><<<gc, 256, WySmem<D>::bytes, stream>>>(group, a.k, a.v, a.beta, vg, vdvp, vdw,
                                                       vdkh, w.dga, w.sdot, a.dv, a.dbeta, a.dg,
-                                                      a.chunks, a.n_chunks, s.H);
+                                                      a.chunks, a.n_chunks, s.H, vec);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (group > 1) {
     k_bwd_heads<<<dim3((unsigned)s.chunk_cap, (unsigned)s.Hk), 256, 0, stream>>>(

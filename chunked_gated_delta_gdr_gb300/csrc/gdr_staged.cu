@@ -1,7 +1,8 @@
 // gdr_staged.cu -- the three stages of the chunked gated delta rule forward as
 // separate kernels with their intermediates in HBM (GDR_PATH_STAGED and the
-// per-stage entry points).  Plain fp32 SIMT arithmetic over shared-memory
-// tiles; bf16 at the same storage points as the fused path (W, U, V', h).
+// per-stage entry points).  fp32 arithmetic over shared-memory tiles (the state
+// scan's products as tf32 tensor-core warp tiles, the rest SIMT); bf16 at the same
+// storage points as the fused path (W, U, V', h).
 //
 // Per chunk of 64 tokens (chunk-local indices i, j) and value head:
 //   stage 1  G = cumsum(g);  A_ij = beta_i e^{G_i-G_j} k_i.k_j (j<i);  Tm = (I+A)^-1
@@ -12,6 +13,7 @@
 // the chunk size is the 64 of FlashQLA's varlen path ("Findings from
 // integrating FlashQLA's Blackwell GDN kernels into a JAX trainer", section 1).
 #include "gdr_internal.cuh"
+#include "gdr_mma.cuh"
 
 namespace gdr {
 namespace {
@@ -19,35 +21,27 @@ namespace {
 // ---------------------------------------------------------------- stage 1
 template <int D>
 struct PrepSmem {
-  static constexpr int kLd = D + 1;
+  static constexpr int kLd = ld_rows(D), kLdA = ld_rows(64);
   static constexpr size_t bytes =
-      sizeof(float) * (2 * 64 * kLd + 2 * 64 * 65 + 3 * 64);
+      sizeof(float) * (2 * 64 * kLd + 3 * 64 * kLdA + 3 * 64 + kSolveScratch);
 };
 
 template <int D>
 __global__ void __launch_bounds__(256)
     k_prep(int32_t group, View k, View v, View g, View beta, View w, View u, View gcum,
-           const ChunkInfo *__restrict__ chunks, const int32_t *__restrict__ n_chunks) {
+           const ChunkInfo *__restrict__ chunks, const int32_t *__restrict__ n_chunks, bool vec) {
   extern __shared__ float sm[];
-  constexpr int L = PrepSmem<D>::kLd;
+  constexpr int L = PrepSmem<D>::kLd, LA = PrepSmem<D>::kLdA;
   const int cid = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   if (cid >= *n_chunks) return;
   const ChunkInfo ci = chunks[cid];
   const int len = ci.len, hk = h / group;
   const int64_t t0 = ci.start;
-  float *Ks = sm, *Vs = Ks + 64 * L, *Am = Vs + 64 * L, *Tm = Am + 64 * 65;
-  float *G = Tm + 64 * 65, *B = G + 64, *BG = B + 64;
+  float *Ks = sm, *Vs = Ks + 64 * L, *Am = Vs + 64 * L, *Tm = Am + 64 * LA, *TU = Tm + 64 * LA;
+  float *G = TU + 64 * LA, *B = G + 64, *BG = B + 64, *scratch = BG + 64;
 
-  for (int idx = tid; idx < 64 * D; idx += blockDim.x) {
-    const int i = idx / D, d = idx % D;
-    float kv = 0.f, vv = 0.f;
-    if (i < len) {
-      kv = ldbf(k.p, (t0 + i) * k.st + hk * k.sh + d);
-      vv = ldbf(v.p, (t0 + i) * v.st + h * v.sh + d);
-    }
-    Ks[i * L + d] = kv;
-    Vs[i * L + d] = vv;
-  }
+  tile_bf16<64, D, 256>(Ks, L, bf_row(k, t0, hk), k.st, len, vec);
+  tile_bf16<64, D, 256>(Vs, L, bf_row(v, t0, h), v.st, len, vec);
   if (tid < 64) {
     G[tid] = tid < len ? ldf(g.p, (t0 + tid) * g.st + h * g.sh) : 0.f;
     B[tid] = tid < len ? ldbf(beta.p, (t0 + tid) * beta.st + h * beta.sh) : 0.f;
@@ -67,38 +61,41 @@ __global__ void __launch_bounds__(256)
   }
   __syncthreads();
   if (tid < 64) BG[tid] = B[tid] * expf(G[tid]);
+  const int warp = tid >> 5;
+  // A_ij = beta_i e^{G_i - G_j} k_i . k_j (j < i): 32 tiles of the key products
+  for (int tl = warp * 4; tl < warp * 4 + 4; ++tl) {
+    const int m0 = (tl >> 3) * 16, n0 = (tl & 7) * 8;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_16x8(acc, SMat{Ks, L, 1}, m0, SMat{Ks, 1, L}, n0, 0, D);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = acc_row(m0, e), j = acc_col(n0, e);
+      Am[i * LA + j] = (j < i && i < len) ? B[i] * expf(G[i] - G[j]) * acc[e] : 0.f;
+    }
+  }
+  __syncthreads();
+  solve_unit_lower64(Am, LA, Tm, LA, scratch);  // Tm = (I + A)^-1
+  // Tm diag(beta e^G) into Am's place, Tm diag(beta) into TU
   for (int idx = tid; idx < 64 * 64; idx += blockDim.x) {
-    const int i = idx / 64, j = idx % 64;
-    float a = 0.f;
-    if (j < i && i < len) {
-      float dot = 0.f;
-#pragma unroll 8
-      for (int d = 0; d < D; ++d) dot += Ks[i * L + d] * Ks[j * L + d];
-      a = B[i] * expf(G[i] - G[j]) * dot;
-    }
-    Am[i * 65 + j] = a;
+    const int i = idx >> 6, j = idx & 63;
+    Am[i * LA + j] = Tm[i * LA + j] * BG[j];
+    TU[i * LA + j] = Tm[i * LA + j] * B[j];
   }
   __syncthreads();
-  if (tid < 64) {  // column c of (I + A)^-1 by forward substitution
-    const int c = tid;
-    for (int i = 0; i < 64; ++i) {
-      float x = (i == c) ? 1.f : 0.f;
-      for (int j = c; j < i; ++j) x -= Am[i * 65 + j] * Tm[j * 65 + c];
-      Tm[i * 65 + c] = x;
+  // W = Tm diag(beta e^G) K, U = Tm diag(beta) V: 64 x D outputs each
+  for (int tl = warp; tl < 4 * (D / 8); tl += 8) {
+    const int m0 = (tl & 3) * 16, n0 = (tl >> 2) * 8;
+    float wa[4] = {0.f, 0.f, 0.f, 0.f}, ua[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_16x8(wa, SMat{Am, LA, 1}, m0, SMat{Ks, L, 1}, n0, 0, 64);
+    mma_16x8(ua, SMat{TU, LA, 1}, m0, SMat{Vs, L, 1}, n0, 0, 64);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = acc_row(m0, e), d = acc_col(n0, e);
+      if (i < len) {
+        stbf(w.p, (t0 + i) * w.st + h * w.sh + d, wa[e]);
+        stbf(u.p, (t0 + i) * u.st + h * u.sh + d, ua[e]);
+      }
     }
-  }
-  __syncthreads();
-  for (int idx = tid; idx < 64 * D; idx += blockDim.x) {
-    const int i = idx / D, d = idx % D;
-    if (i >= len) continue;
-    float wa = 0.f, ua = 0.f;
-    for (int j = 0; j <= i; ++j) {
-      const float t = Tm[i * 65 + j];
-      wa += t * BG[j] * Ks[j * L + d];
-      ua += t * B[j] * Vs[j * L + d];
-    }
-    stbf(w.p, (t0 + i) * w.st + h * w.sh + d, wa);
-    stbf(u.p, (t0 + i) * u.st + h * u.sh + d, ua);
   }
   if (tid < len) reinterpret_cast<float *>(gcum.p)[(t0 + tid) * gcum.st + h * gcum.sh] = G[tid];
 }
@@ -108,28 +105,28 @@ constexpr int kScanCols = 32;  // value columns of S per block
 
 template <int D>
 struct ScanSmem {
-  static constexpr int kLd = D + 1;
+  static constexpr int kLdW = ld_rows(D), kLdK = ld_cols(D), kLdC = ld_cols(kScanCols);
   static constexpr size_t bytes =
-      sizeof(float) * (D * 33 + 2 * 64 * kLd + 2 * 64 * 33 + 2 * 64);
+      sizeof(float) * (D * kLdC + 64 * kLdW + 64 * kLdK + 2 * 64 * kLdC + 2 * 64);
 };
 
 template <int D>
 __global__ void __launch_bounds__(128)
     k_scan(int32_t H, int32_t group, View k, View w, View u, View gcum, const float *h0,
            __nv_bfloat16 *hbuf, View v_new, float *ht, Ckpt ck,
-           const SegInfo *__restrict__ seg) {
+           const SegInfo *__restrict__ seg, bool vec) {
   extern __shared__ float sm[];
-  constexpr int L = ScanSmem<D>::kLd;
+  constexpr int LW = ScanSmem<D>::kLdW, LK = ScanSmem<D>::kLdK, LC = ScanSmem<D>::kLdC;
   const int n = blockIdx.x, h = blockIdx.y, jb = blockIdx.z * kScanCols, tid = threadIdx.x;
   const int hk = h / group;
   const SegInfo si = seg[n];
-  float *S = sm, *Ws = S + D * 33, *Ks = Ws + 64 * L, *Us = Ks + 64 * L, *Vn = Us + 64 * 33;
-  float *G = Vn + 64 * 33, *Dec = G + 64;
+  float *S = sm, *Ws = S + D * LC, *Ks = Ws + 64 * LW, *Us = Ks + 64 * LK, *Vn = Us + 64 * LC;
+  float *G = Vn + 64 * LC, *Dec = G + 64;
   const int64_t sbase = ((int64_t)n * H + h) * D * D;
 
   for (int idx = tid; idx < D * kScanCols; idx += blockDim.x) {
     const int d = idx / kScanCols, j = idx % kScanCols;
-    S[d * 33 + j] = h0 ? h0[sbase + (int64_t)d * D + jb + j] : 0.f;
+    S[d * LC + j] = h0 ? h0[sbase + (int64_t)d * D + jb + j] : 0.f;
   }
   // state of this block's columns -> checkpoint row `row` (the state after the
   // segment's first (row - first row + 1) * every tokens)
@@ -137,7 +134,7 @@ __global__ void __launch_bounds__(128)
     float *dst = ck.h + (row * H + h) * D * D;
     for (int idx = tid; idx < D * kScanCols; idx += blockDim.x) {
       const int d = idx / kScanCols, j = idx % kScanCols;
-      dst[(int64_t)d * D + jb + j] = S[d * 33 + j];
+      dst[(int64_t)d * D + jb + j] = S[d * LC + j];
     }
   };
   for (int c = 0; c < si.n_chunks; ++c) {
@@ -150,53 +147,57 @@ __global__ void __launch_bounds__(128)
     __nv_bfloat16 *hc = hbuf + (cid * H + h) * D * D;
     for (int idx = tid; idx < D * kScanCols; idx += blockDim.x) {
       const int d = idx / kScanCols, j = idx % kScanCols;
-      hc[(int64_t)d * D + jb + j] = __float2bfloat16_rn(S[d * 33 + j]);
+      hc[(int64_t)d * D + jb + j] = __float2bfloat16_rn(S[d * LC + j]);
     }
-    for (int idx = tid; idx < 64 * D; idx += blockDim.x) {
-      const int i = idx / D, d = idx % D;
-      float wv = 0.f, kv = 0.f;
-      if (i < len) {
-        wv = ldbf(w.p, (t0 + i) * w.st + h * w.sh + d);
-        kv = ldbf(k.p, (t0 + i) * k.st + hk * k.sh + d);
-      }
-      Ws[i * L + d] = wv;
-      Ks[i * L + d] = kv;
-    }
-    for (int idx = tid; idx < 64 * kScanCols; idx += blockDim.x) {
-      const int i = idx / kScanCols, j = idx % kScanCols;
-      Us[i * 33 + j] = i < len ? ldbf(u.p, (t0 + i) * u.st + h * u.sh + jb + j) : 0.f;
-    }
+    tile_bf16<64, D, 128>(Ws, LW, bf_row(w, t0, h),
+                          w.st, len, vec);
+    tile_bf16<64, D, 128>(Ks, LK, bf_row(k, t0, hk), k.st, len, vec);
+    tile_bf16<64, kScanCols, 128>(
+        Us, LC, bf_row(u, t0, h) + jb, u.st, len,
+        vec);
     if (tid < 64) G[tid] = tid < len ? ldf(gcum.p, (t0 + tid) * gcum.st + h * gcum.sh) : 0.f;
     __syncthreads();
     const float glast = G[len - 1];
     if (tid < 64) Dec[tid] = tid < len ? expf(glast - G[tid]) : 0.f;
-    for (int idx = tid; idx < 64 * kScanCols; idx += blockDim.x) {
-      const int i = idx / kScanCols, j = idx % kScanCols;
-      float vn = 0.f;
-      if (i < len) {
-        float acc = Us[i * 33 + j];
-#pragma unroll 8
-        for (int d = 0; d < D; ++d) acc -= Ws[i * L + d] * S[d * 33 + j];
-        const __nv_bfloat16 b = __float2bfloat16_rn(acc);
-        reinterpret_cast<__nv_bfloat16 *>(v_new.p)[(t0 + i) * v_new.st + h * v_new.sh + jb + j] = b;
-        vn = __bfloat162float(b);
+    __syncthreads();
+    const int warp = tid >> 5;
+    // V' = U - W S (bf16, as stored), and Vn = diag(e^{G_last - G}) V' for the update:
+    // 64 x 32 outputs, four 16 x 8 tiles per warp on the tensor pipe
+    for (int tl = warp * 4; tl < warp * 4 + 4; ++tl) {
+      const int m0 = (tl >> 2) * 16, n0 = (tl & 3) * 8;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_16x8(acc, SMat{Ws, LW, 1}, m0, SMat{S, LC, 1}, n0, 0, D);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = acc_row(m0, e), j = acc_col(n0, e);
+        float vn = 0.f;
+        if (i < len) {
+          const __nv_bfloat16 b = __float2bfloat16_rn(Us[i * LC + j] - acc[e]);
+          reinterpret_cast<__nv_bfloat16 *>(v_new.p)[(t0 + i) * v_new.st + h * v_new.sh + jb + j] = b;
+          vn = Dec[i] * __bfloat162float(b);
+        }
+        Vn[i * LC + j] = vn;
       }
-      Vn[i * 33 + j] = vn;
     }
     __syncthreads();
+    // S <- e^{G_last} S + K^T Vn: D x 32 outputs
     const float eg = expf(glast);
-    for (int idx = tid; idx < D * kScanCols; idx += blockDim.x) {
-      const int d = idx / kScanCols, j = idx % kScanCols;
-      float acc = eg * S[d * 33 + j];
-      for (int i = 0; i < len; ++i) acc += Dec[i] * Ks[i * L + d] * Vn[i * 33 + j];
-      S[d * 33 + j] = acc;
+    for (int tl = warp; tl < (D / 16) * 4; tl += 4) {
+      const int m0 = (tl >> 2) * 16, n0 = (tl & 3) * 8;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_16x8(acc, SMat{Ks, 1, LK}, m0, SMat{Vn, LC, 1}, n0, 0, 64);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int d = acc_row(m0, e), j = acc_col(n0, e);
+        S[d * LC + j] = eg * S[d * LC + j] + acc[e];
+      }
     }
   }
   if (ht || ck.h) __syncthreads();
   if (ht) {
     for (int idx = tid; idx < D * kScanCols; idx += blockDim.x) {
       const int d = idx / kScanCols, j = idx % kScanCols;
-      ht[sbase + (int64_t)d * D + jb + j] = S[d * 33 + j];
+      ht[sbase + (int64_t)d * D + jb + j] = S[d * LC + j];
     }
   }
   const int seg_len = si.end - si.start;
@@ -208,45 +209,32 @@ constexpr int kOutCols = 64;
 
 template <int D>
 struct OutSmem {
-  static constexpr int kLd = D + 1;
+  static constexpr int kLd = ld_rows(D), kLdH = ld_rows(kOutCols);
   static constexpr size_t bytes =
-      sizeof(float) * (2 * 64 * kLd + D * 65 + 2 * 64 * 65 + 64);
+      sizeof(float) * (2 * 64 * kLd + D * kLdH + 64 * kLdH + 64 * 65 + 64);
 };
 
 template <int D>
 __global__ void __launch_bounds__(256)
     k_out(int32_t H, int32_t group, View q, View k, View v_new, const __nv_bfloat16 *hbuf,
           View gcum, float scale, View o, const ChunkInfo *__restrict__ chunks,
-          const int32_t *__restrict__ n_chunks) {
+          const int32_t *__restrict__ n_chunks, bool vec) {
   extern __shared__ float sm[];
-  constexpr int L = OutSmem<D>::kLd;
+  constexpr int L = OutSmem<D>::kLd, LH = OutSmem<D>::kLdH;
   const int cid = blockIdx.x, h = blockIdx.y, cb = blockIdx.z * kOutCols, tid = threadIdx.x;
   if (cid >= *n_chunks) return;
   const ChunkInfo ci = chunks[cid];
   const int len = ci.len, hk = h / group;
   const int64_t t0 = ci.start;
-  float *Qs = sm, *Ks = Qs + 64 * L, *Hs = Ks + 64 * L, *Vn = Hs + D * 65, *P = Vn + 64 * 65;
+  float *Qs = sm, *Ks = Qs + 64 * L, *Hs = Ks + 64 * L, *Vn = Hs + D * LH, *P = Vn + 64 * LH;
   float *G = P + 64 * 65;
 
-  for (int idx = tid; idx < 64 * D; idx += blockDim.x) {
-    const int i = idx / D, d = idx % D;
-    float qv = 0.f, kv = 0.f;
-    if (i < len) {
-      qv = ldbf(q.p, (t0 + i) * q.st + hk * q.sh + d);
-      kv = ldbf(k.p, (t0 + i) * k.st + hk * k.sh + d);
-    }
-    Qs[i * L + d] = qv;
-    Ks[i * L + d] = kv;
-  }
+  tile_bf16<64, D, 256>(Qs, L, bf_row(q, t0, hk), q.st, len, vec);
+  tile_bf16<64, D, 256>(Ks, L, bf_row(k, t0, hk), k.st, len, vec);
   const __nv_bfloat16 *hc = hbuf + ((int64_t)cid * H + h) * D * D;
-  for (int idx = tid; idx < D * kOutCols; idx += blockDim.x) {
-    const int d = idx / kOutCols, c = idx % kOutCols;
-    Hs[d * 65 + c] = __bfloat162float(hc[(int64_t)d * D + cb + c]);
-  }
-  for (int idx = tid; idx < 64 * kOutCols; idx += blockDim.x) {
-    const int i = idx / kOutCols, c = idx % kOutCols;
-    Vn[i * 65 + c] = i < len ? ldbf(v_new.p, (t0 + i) * v_new.st + h * v_new.sh + cb + c) : 0.f;
-  }
+  tile_bf16<D, kOutCols, 256>(Hs, LH, hc + cb, D, D, vec);
+  tile_bf16<64, kOutCols, 256>(Vn, LH, bf_row(v_new, t0, h) + cb,
+                               v_new.st, len, vec);
   if (tid < 64) G[tid] = tid < len ? ldf(gcum.p, (t0 + tid) * gcum.st + h * gcum.sh) : 0.f;
   __syncthreads();
   for (int idx = tid; idx < 64 * 64; idx += blockDim.x) {
@@ -266,11 +254,16 @@ __global__ void __launch_bounds__(256)
     if (i >= len) continue;
     float inter = 0.f, intra = 0.f;
 #pragma unroll 8
-    for (int d = 0; d < D; ++d) inter += Qs[i * L + d] * Hs[d * 65 + c];
-    for (int j = 0; j <= i; ++j) intra += P[i * 65 + j] * Vn[j * 65 + c];
+    for (int d = 0; d < D; ++d) inter += Qs[i * L + d] * Hs[d * LH + c];
+    for (int j = 0; j <= i; ++j) intra += P[i * 65 + j] * Vn[j * LH + c];
     const float r = scale * (expf(G[i]) * inter + intra);
     stbf(o.p, (t0 + i) * o.st + h * o.sh + cb + c, r);
   }
+}
+
+// 16-byte vector loads of a caller's bf16 tensor when its rows allow it
+bool vec_ok(const View &x) {
+  return (reinterpret_cast<uintptr_t>(x.p) & 15) == 0 && x.st % 8 == 0 && x.sh % 8 == 0;
 }
 
 template <typename K>
@@ -285,15 +278,16 @@ cudaError_t launch_prep(const StageShapes &s, View k, View v, View g, View beta,
                         const int32_t *n_chunks, cudaStream_t stream) {
   if (s.chunk_cap <= 0 || s.H <= 0) return cudaSuccess;
   dim3 grid((unsigned)s.chunk_cap, (unsigned)s.H);
+  const bool vec = vec_ok(k) && vec_ok(v);
   cudaError_t e;
   if (s.D == 64) {
     if ((e = set_smem(k_prep<64>, PrepSmem<64>::bytes)) != cudaSuccess) return e;
     k_prep<64><<<grid, 256, PrepSmem<64>::bytes, stream>>>(s.H / s.Hk, k, v, g, beta, w, u,
-                                                           gcum, chunks, n_chunks);
+                                                           gcum, chunks, n_chunks, vec);
   } else {
     if ((e = set_smem(k_prep<128>, PrepSmem<128>::bytes)) != cudaSuccess) return e;
     k_prep<128><<<grid, 256, PrepSmem<128>::bytes, stream>>>(s.H / s.Hk, k, v, g, beta, w, u,
-                                                             gcum, chunks, n_chunks);
+                                                             gcum, chunks, n_chunks, vec);
   }
   return cudaGetLastError();
 }
@@ -304,15 +298,16 @@ cudaError_t launch_scan(const StageShapes &s, View k, View w, View u, View gcum,
   if (s.n_seq <= 0 || s.H <= 0) return cudaSuccess;
   dim3 grid((unsigned)s.n_seq, (unsigned)s.H, (unsigned)(s.D / kScanCols));
   auto *hb = reinterpret_cast<__nv_bfloat16 *>(h);
+  const bool vec = vec_ok(k) && vec_ok(w) && vec_ok(u);
   cudaError_t e;
   if (s.D == 64) {
     if ((e = set_smem(k_scan<64>, ScanSmem<64>::bytes)) != cudaSuccess) return e;
     k_scan<64><<<grid, 128, ScanSmem<64>::bytes, stream>>>(s.H, s.H / s.Hk, k, w, u, gcum, h0,
-                                                           hb, v_new, ht, ck, seg);
+                                                           hb, v_new, ht, ck, seg, vec);
   } else {
     if ((e = set_smem(k_scan<128>, ScanSmem<128>::bytes)) != cudaSuccess) return e;
     k_scan<128><<<grid, 128, ScanSmem<128>::bytes, stream>>>(s.H, s.H / s.Hk, k, w, u, gcum,
-                                                             h0, hb, v_new, ht, ck, seg);
+                                                             h0, hb, v_new, ht, ck, seg, vec);
   }
   return cudaGetLastError();
 }
@@ -323,15 +318,17 @@ cudaError_t launch_out(const StageShapes &s, View q, View k, View v_new, const v
   if (s.chunk_cap <= 0 || s.H <= 0) return cudaSuccess;
   dim3 grid((unsigned)s.chunk_cap, (unsigned)s.H, (unsigned)(s.D / kOutCols));
   auto *hb = reinterpret_cast<const __nv_bfloat16 *>(h);
+  const bool vec = vec_ok(q) && vec_ok(k) && vec_ok(v_new) &&
+                   (reinterpret_cast<uintptr_t>(h) & 15) == 0;
   cudaError_t e;
   if (s.D == 64) {
     if ((e = set_smem(k_out<64>, OutSmem<64>::bytes)) != cudaSuccess) return e;
     k_out<64><<<grid, 256, OutSmem<64>::bytes, stream>>>(s.H, s.H / s.Hk, q, k, v_new, hb,
-                                                         gcum, scale, o, chunks, n_chunks);
+                                                         gcum, scale, o, chunks, n_chunks, vec);
   } else {
     if ((e = set_smem(k_out<128>, OutSmem<128>::bytes)) != cudaSuccess) return e;
     k_out<128><<<grid, 256, OutSmem<128>::bytes, stream>>>(s.H, s.H / s.Hk, q, k, v_new, hb,
-                                                           gcum, scale, o, chunks, n_chunks);
+                                                           gcum, scale, o, chunks, n_chunks, vec);
   }
   return cudaGetLastError();
 }
