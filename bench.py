@@ -396,8 +396,8 @@ def bench_e2e(args, api, w, dev, path, dist):
             "timed": "host wall clock around the public chunk_fwd call on pinned host tensors"}
 
 
-METRIC_BWD = "GDR chunk-bwd tokens/s (H=32, d=128, 64k packed) & % of fp32 SIMT roofline"
-SM_COUNT, FP32_LANES_PER_SM = 152, 128
+METRIC_BWD = "GDR chunk-bwd tokens/s (H=32, d=128, 64k packed) & % of tf32 tensor roofline"
+TF32_PER_BF16 = 1.1 / 2.25
 
 
 def algorithmic_flops_bwd(w) -> int:
@@ -424,11 +424,6 @@ def algorithmic_bytes_bwd(w) -> int:
     states = w.n_seq * H * dk * dv * 4
     b += states * ((w.h0 is not None) * 2 + bool(w.want_ht))
     return b
-
-
-def fp32_simt_peak_tflops(sm_mhz: float) -> float:
-    """152 SMs x 128 FP32 lanes x 2 FLOP per FMA x the SM clock."""
-    return SM_COUNT * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
 
 
 def _upstream_bwd(w, dev):
@@ -487,9 +482,10 @@ def bench_ours_bwd(args):
     med_ms = statistics.median(per)
     flops = algorithmic_flops_bwd(w)
     byts = algorithmic_bytes_bwd(w)
-    sm_mhz = (clocks or {}).get("sm_max_mhz") or 2070.0
-    peak = fp32_simt_peak_tflops(sm_mhz)
-    hbm, _, peak_kind = peaks()
+    hbm, bf16_tf, peak_kind = peaks()
+    # the dense products run as tf32 tensor-core tiles: the tf32 peak is the measured
+    # bf16 peak times the nominal tf32 / bf16 ratio (1.1 / 2.25 PFLOP/s dense)
+    peak = bf16_tf * TF32_PER_BF16
     achieved = flops / (med_ms / 1e3) / 1e12
     # chunk enumeration (2), forward recompute (2), five backward kernels, grouped heads
     launches = 2 + 2 + 5 + (w.H != w.Hk)
@@ -501,9 +497,9 @@ def bench_ours_bwd(args):
                        "d": w.dk, "n_seq": w.n_seq, "n_chunks": w.n_chunks(),
                        "upstream": "dout = 0.1 N(0,1) bf16" + (", dht = 0.1 N(0,1)" if dht is not None else ""),
                        "l2": "inputs and fp32 gradients exceed the 129 MB L2; no flush between steps"},
-            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak,
-                         "peak_kind": "derived: 152 SMs x 128 FP32 lanes x 2 FLOP x SM clock",
+                         "peak_kind": f"{peak_kind} bf16 burst x nominal tf32/bf16 ratio 1.1/2.25",
                          "traffic": None, "algorithmic_flops_per_launch": flops,
                          "hbm": {"algorithmic_bytes_per_launch": byts,
                                  "achieved_gbs": byts / (med_ms / 1e3) / 1e9, "peak": hbm,

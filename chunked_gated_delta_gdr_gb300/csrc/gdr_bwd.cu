@@ -94,22 +94,24 @@ __global__ void __launch_bounds__(256)
 }
 
 // ---------------------------------------------------------------- reverse state scan
-constexpr int kScanCols = 32;
 
-template <int D>
+template <int D, int kScanCols>
 struct BwdScanSmem {
   static constexpr int kLdK = ld_rows(D), kLdQ = ld_cols(D), kLdC = ld_cols(kScanCols);
   static constexpr size_t bytes =
       sizeof(float) * (D * kLdC + 64 * kLdK + 2 * 64 * kLdQ + 2 * 64 * kLdC + 3 * 64);
 };
 
-template <int D>
-__global__ void __launch_bounds__(128)
+// kScanCols value columns per block, kScanCols / 8 warps
+template <int D, int kScanCols>
+__global__ void __launch_bounds__(kScanCols * 4)
     k_bwd_scan(int32_t H, int32_t group, View q, View k, View w, View dout, View gcum,
                float scale, const float *dht, View dvp, float *dh, float *dh0,
                const SegInfo *__restrict__ seg, bool vec) {
   extern __shared__ float sm[];
-  constexpr int LK = BwdScanSmem<D>::kLdK, LQ = BwdScanSmem<D>::kLdQ, LC = BwdScanSmem<D>::kLdC;
+  using Sm = BwdScanSmem<D, kScanCols>;
+  constexpr int LK = Sm::kLdK, LQ = Sm::kLdQ, LC = Sm::kLdC;
+  constexpr int NT = kScanCols * 4, NW = kScanCols / 8, CT = kScanCols / 8;  // threads, warps, column tiles
   const int n = blockIdx.x, h = blockIdx.y, jb = blockIdx.z * kScanCols, tid = threadIdx.x;
   const int hk = h / group;
   const SegInfo si = seg[n];
@@ -131,12 +133,12 @@ __global__ void __launch_bounds__(128)
       const int d = idx / kScanCols, j = idx % kScanCols;
       dhc[(int64_t)d * D + jb + j] = dS[d * LC + j];
     }
-    tile_bf16<64, D, 128>(Ks, LK, bf_row(k, t0, hk), k.st, len, vec);
-    tile_bf16<64, D, 128>(Ws, LQ, bf_row(w, t0, h), w.st, len, true);
-    tile_bf16<64, D, 128>(Qs, LQ, bf_row(q, t0, hk), q.st, len, vec);
-    tile_bf16<64, kScanCols, 128>(Dos, LC, bf_row(dout, t0, h) + jb,
+    tile_bf16<64, D, NT>(Ks, LK, bf_row(k, t0, hk), k.st, len, vec);
+    tile_bf16<64, D, NT>(Ws, LQ, bf_row(w, t0, h), w.st, len, true);
+    tile_bf16<64, D, NT>(Qs, LQ, bf_row(q, t0, hk), q.st, len, vec);
+    tile_bf16<64, kScanCols, NT>(Dos, LC, bf_row(dout, t0, h) + jb,
                                   dout.st, len, vec);
-    tile_f32<64, kScanCols, 128>(Vd, LC, dvt + t0 * dvp.st + h * dvp.sh + jb, dvp.st, len);
+    tile_f32<64, kScanCols, NT>(Vd, LC, dvt + t0 * dvp.st + h * dvp.sh + jb, dvp.st, len);
     if (tid < 64) G[tid] = tid < len ? ldf(gcum.p, (t0 + tid) * gcum.st + h * gcum.sh) : 0.f;
     __syncthreads();
     const float glast = G[len - 1];
@@ -148,9 +150,9 @@ __global__ void __launch_bounds__(128)
     for (int idx = tid; idx < 64 * kScanCols; idx += blockDim.x)  // dO <- diag(e^G) dO
       Dos[(idx / kScanCols) * LC + idx % kScanCols] *= EG[idx / kScanCols];
     const int warp = tid >> 5;
-    // dV' = dV'_intra + diag(e^{G_C - G}) K dS_C: 16 tiles, four per warp
+    // dV' = dV'_intra + diag(e^{G_C - G}) K dS_C: 4 x CT tiles, four per warp
     for (int tl = warp * 4; tl < warp * 4 + 4; ++tl) {
-      const int m0 = (tl >> 2) * 16, n0 = (tl & 3) * 8;
+      const int m0 = (tl / CT) * 16, n0 = (tl % CT) * 8;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       mma_16x8(acc, SMat{Ks, LK, 1}, m0, SMat{dS, LC, 1}, n0, 0, D);
 #pragma unroll
@@ -164,10 +166,10 @@ __global__ void __launch_bounds__(128)
       }
     }
     __syncthreads();
-    // dS_0 = e^{G_C} dS_C + scale Q^T diag(e^G) dO - W^T dV': D/16 x 4 tiles over 4 warps
+    // dS_0 = e^{G_C} dS_C + scale Q^T diag(e^G) dO - W^T dV': D/16 x CT tiles
     const float eg = expf(glast);
-    for (int tl = warp; tl < (D / 16) * 4; tl += 4) {
-      const int m0 = (tl >> 2) * 16, n0 = (tl & 3) * 8;
+    for (int tl = warp; tl < (D / 16) * CT; tl += NW) {
+      const int m0 = (tl / CT) * 16, n0 = (tl % CT) * 8;
       float inj[4] = {0.f, 0.f, 0.f, 0.f}, corr[4] = {0.f, 0.f, 0.f, 0.f};
       mma_16x8(inj, SMat{Qs, 1, LQ}, m0, SMat{Dos, LC, 1}, n0, 0, 64);
       mma_16x8(corr, SMat{Ws, 1, LQ}, m0, SMat{Vd, LC, 1}, n0, 0, 64);
@@ -188,7 +190,7 @@ __global__ void __launch_bounds__(128)
 }
 
 // ---------------------------------------------------------------- products with S_0, dS_C
-constexpr int kSRows = 32;  // key rows of S_0 / dS_C per block
+constexpr int kSRows = 64;  // key rows of S_0 / dS_C per block
 
 template <int D>
 struct SgradSmem {
@@ -230,10 +232,10 @@ __global__ void __launch_bounds__(256)
   __syncthreads();
   float *q_out = reinterpret_cast<float *>(dqh.p), *k_out = reinterpret_cast<float *>(dkh.p);
   float *w_out = reinterpret_cast<float *>(dw.p);
-  // 64 x 32 outputs of each product: 16 tiles, two per warp
+  // 64 x kSRows outputs of each product: 32 tiles, four per warp
   const int warp = tid >> 5;
-  for (int tl = warp * 2; tl < warp * 2 + 2; ++tl) {
-    const int m0 = (tl >> 2) * 16, n0 = (tl & 3) * 8;
+  for (int tl = warp * 4; tl < warp * 4 + 4; ++tl) {
+    const int m0 = (tl >> 3) * 16, n0 = (tl & 7) * 8;
     float aq[4] = {0.f, 0.f, 0.f, 0.f}, ak[4] = {0.f, 0.f, 0.f, 0.f}, aw[4] = {0.f, 0.f, 0.f, 0.f};
     mma_16x8(aq, SMat{Dos, L, 1}, m0, SMat{S0, 1, L}, n0, 0, D);
     mma_16x8(ak, SMat{Vp, L, 1}, m0, SMat{dS, 1, L}, n0, 0, D);
@@ -649,12 +651,16 @@ cudaError_t launch_bwd_d(const BwdArgs &a, const BwdWs &w, cudaStream_t stream) 
   k_bwd_dv_intra<D><<<dim3(gc.x, gc.y, D / 64), 256, DvIntraSmem<D>::bytes, stream>>>(
       group, a.q, a.k, a.dout, vg, a.scale, vdvp, a.chunks, a.n_chunks, vec);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if ((e = set_smem(k_bwd_scan<D>, BwdScanSmem<D>::bytes)) != cudaSuccess) return e;
-  k_bwd_scan<D><<<dim3((unsigned)s.n_seq, (unsigned)s.H, D / kScanCols), 128,
-                  BwdScanSmem<D>::bytes, stream>>>(s.H, group, a.q, a.k, vw, a.dout, vg,
-                                                   a.scale, a.dht, vdvp, w.dh, a.dh0, a.seg,
-                                                   vec);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  auto scan = [&](auto kern, int cols, size_t bytes) -> cudaError_t {
+    cudaError_t r = set_smem(kern, bytes);
+    if (r != cudaSuccess) return r;
+    kern<<<dim3((unsigned)s.n_seq, (unsigned)s.H, (unsigned)(D / cols)), cols * 4, bytes, stream>>>(
+        s.H, group, a.q, a.k, vw, a.dout, vg, a.scale, a.dht, vdvp, w.dh, a.dh0, a.seg, vec);
+    return cudaGetLastError();
+  };
+  e = scan_cols(s.n_seq, s.H, D) == 64 ? scan(k_bwd_scan<D, 64>, 64, BwdScanSmem<D, 64>::bytes)
+                                       : scan(k_bwd_scan<D, 32>, 32, BwdScanSmem<D, 32>::bytes);
+  if (e != cudaSuccess) return e;
   if ((e = set_smem(k_bwd_sgrad<D>, SgradSmem<D>::bytes)) != cudaSuccess) return e;
   k_bwd_sgrad<D><<<dim3(gc.x, gc.y, D / kSRows), 256, SgradSmem<D>::bytes, stream>>>(
       a.dout, vn, vg, a.scale, reinterpret_cast<const __nv_bfloat16 *>(w.h), w.dh, vdvp, vdqh,

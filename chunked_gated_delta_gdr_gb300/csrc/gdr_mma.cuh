@@ -10,6 +10,21 @@
 
 namespace gdr {
 
+// Streaming multiprocessors of the current device (cached; 0 if it cannot be queried).
+inline int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev] == 0) cudaDeviceGetAttribute(&cache[dev], cudaDevAttrMultiProcessorCount, dev);
+  return cache[dev];
+}
+
+// Value columns per block of a sequential scan over (segment, head) pairs: 64 (eight
+// warps) when that still gives every SM a block, else 32 (four warps, twice the blocks).
+inline int scan_cols(int64_t n_seq, int64_t H, int D) {
+  return n_seq * H * (D / 64) >= device_sm_count() ? 64 : 32;
+}
+
 // Row t, head `head` of a bf16 [rows, heads, dim] view.
 __device__ __forceinline__ const __nv_bfloat16 *bf_row(const View &x, int64_t t, int64_t head) {
   return reinterpret_cast<const __nv_bfloat16 *>(x.p) + t * x.st + head * x.sh;

@@ -101,22 +101,24 @@ __global__ void __launch_bounds__(256)
 }
 
 // ---------------------------------------------------------------- stage 2
-constexpr int kScanCols = 32;  // value columns of S per block
 
-template <int D>
+template <int D, int kScanCols>
 struct ScanSmem {
   static constexpr int kLdW = ld_rows(D), kLdK = ld_cols(D), kLdC = ld_cols(kScanCols);
   static constexpr size_t bytes =
       sizeof(float) * (D * kLdC + 64 * kLdW + 64 * kLdK + 2 * 64 * kLdC + 2 * 64);
 };
 
-template <int D>
-__global__ void __launch_bounds__(128)
+// kScanCols value columns per block, kScanCols / 8 warps
+template <int D, int kScanCols>
+__global__ void __launch_bounds__(kScanCols * 4)
     k_scan(int32_t H, int32_t group, View k, View w, View u, View gcum, const float *h0,
            __nv_bfloat16 *hbuf, View v_new, float *ht, Ckpt ck,
            const SegInfo *__restrict__ seg, bool vec) {
   extern __shared__ float sm[];
-  constexpr int LW = ScanSmem<D>::kLdW, LK = ScanSmem<D>::kLdK, LC = ScanSmem<D>::kLdC;
+  using Sm = ScanSmem<D, kScanCols>;
+  constexpr int LW = Sm::kLdW, LK = Sm::kLdK, LC = Sm::kLdC;
+  constexpr int NT = kScanCols * 4, NW = kScanCols / 8, CT = kScanCols / 8;  // threads, warps, column tiles
   const int n = blockIdx.x, h = blockIdx.y, jb = blockIdx.z * kScanCols, tid = threadIdx.x;
   const int hk = h / group;
   const SegInfo si = seg[n];
@@ -149,10 +151,10 @@ __global__ void __launch_bounds__(128)
       const int d = idx / kScanCols, j = idx % kScanCols;
       hc[(int64_t)d * D + jb + j] = __float2bfloat16_rn(S[d * LC + j]);
     }
-    tile_bf16<64, D, 128>(Ws, LW, bf_row(w, t0, h),
+    tile_bf16<64, D, NT>(Ws, LW, bf_row(w, t0, h),
                           w.st, len, vec);
-    tile_bf16<64, D, 128>(Ks, LK, bf_row(k, t0, hk), k.st, len, vec);
-    tile_bf16<64, kScanCols, 128>(
+    tile_bf16<64, D, NT>(Ks, LK, bf_row(k, t0, hk), k.st, len, vec);
+    tile_bf16<64, kScanCols, NT>(
         Us, LC, bf_row(u, t0, h) + jb, u.st, len,
         vec);
     if (tid < 64) G[tid] = tid < len ? ldf(gcum.p, (t0 + tid) * gcum.st + h * gcum.sh) : 0.f;
@@ -162,9 +164,9 @@ __global__ void __launch_bounds__(128)
     __syncthreads();
     const int warp = tid >> 5;
     // V' = U - W S (bf16, as stored), and Vn = diag(e^{G_last - G}) V' for the update:
-    // 64 x 32 outputs, four 16 x 8 tiles per warp on the tensor pipe
+    // 64 x kScanCols outputs, four 16 x 8 tiles per warp on the tensor pipe
     for (int tl = warp * 4; tl < warp * 4 + 4; ++tl) {
-      const int m0 = (tl >> 2) * 16, n0 = (tl & 3) * 8;
+      const int m0 = (tl / CT) * 16, n0 = (tl % CT) * 8;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       mma_16x8(acc, SMat{Ws, LW, 1}, m0, SMat{S, LC, 1}, n0, 0, D);
 #pragma unroll
@@ -180,10 +182,10 @@ __global__ void __launch_bounds__(128)
       }
     }
     __syncthreads();
-    // S <- e^{G_last} S + K^T Vn: D x 32 outputs
+    // S <- e^{G_last} S + K^T Vn: D x kScanCols outputs
     const float eg = expf(glast);
-    for (int tl = warp; tl < (D / 16) * 4; tl += 4) {
-      const int m0 = (tl >> 2) * 16, n0 = (tl & 3) * 8;
+    for (int tl = warp; tl < (D / 16) * CT; tl += NW) {
+      const int m0 = (tl / CT) * 16, n0 = (tl % CT) * 8;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       mma_16x8(acc, SMat{Ks, 1, LK}, m0, SMat{Vn, LC, 1}, n0, 0, 64);
 #pragma unroll
@@ -296,20 +298,21 @@ cudaError_t launch_scan(const StageShapes &s, View k, View w, View u, View gcum,
                         const float *h0, void *h, View v_new, float *ht, Ckpt ck,
                         const SegInfo *seg, cudaStream_t stream) {
   if (s.n_seq <= 0 || s.H <= 0) return cudaSuccess;
-  dim3 grid((unsigned)s.n_seq, (unsigned)s.H, (unsigned)(s.D / kScanCols));
   auto *hb = reinterpret_cast<__nv_bfloat16 *>(h);
   const bool vec = vec_ok(k) && vec_ok(w) && vec_ok(u);
-  cudaError_t e;
-  if (s.D == 64) {
-    if ((e = set_smem(k_scan<64>, ScanSmem<64>::bytes)) != cudaSuccess) return e;
-    k_scan<64><<<grid, 128, ScanSmem<64>::bytes, stream>>>(s.H, s.H / s.Hk, k, w, u, gcum, h0,
-                                                           hb, v_new, ht, ck, seg, vec);
-  } else {
-    if ((e = set_smem(k_scan<128>, ScanSmem<128>::bytes)) != cudaSuccess) return e;
-    k_scan<128><<<grid, 128, ScanSmem<128>::bytes, stream>>>(s.H, s.H / s.Hk, k, w, u, gcum,
-                                                             h0, hb, v_new, ht, ck, seg, vec);
-  }
-  return cudaGetLastError();
+  auto scan = [&](auto kern, int cols, size_t bytes) -> cudaError_t {
+    cudaError_t r = set_smem(kern, bytes);
+    if (r != cudaSuccess) return r;
+    kern<<<dim3((unsigned)s.n_seq, (unsigned)s.H, (unsigned)(s.D / cols)), cols * 4, bytes,
+           stream>>>(s.H, s.H / s.Hk, k, w, u, gcum, h0, hb, v_new, ht, ck, seg, vec);
+    return cudaGetLastError();
+  };
+  const bool wide = scan_cols(s.n_seq, s.H, s.D) == 64;
+  if (s.D == 64)
+    return wide ? scan(k_scan<64, 64>, 64, ScanSmem<64, 64>::bytes)
+                : scan(k_scan<64, 32>, 32, ScanSmem<64, 32>::bytes);
+  return wide ? scan(k_scan<128, 64>, 64, ScanSmem<128, 64>::bytes)
+              : scan(k_scan<128, 32>, 32, ScanSmem<128, 32>::bytes);
 }
 
 cudaError_t launch_out(const StageShapes &s, View q, View k, View v_new, const void *h,
