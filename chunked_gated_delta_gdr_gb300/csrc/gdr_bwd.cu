@@ -68,27 +68,37 @@ __global__ void __launch_bounds__(256)
   __syncthreads();
   const int warp = tid >> 5;
   // P = (Q K^T) o Gam (j <= i): 32 tiles of 16 x 8, four per warp
-  for (int tl = warp * 4; tl < warp * 4 + 4; ++tl) {
-    const int m0 = (tl >> 3) * 16, n0 = (tl & 7) * 8;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    mma_16x8(acc, SMat{Qs, L, 1}, m0, SMat{Ks, 1, L}, n0, 0, D);
+  {
+    const int m0 = ((warp * 4) >> 3) * 16, nb = ((warp * 4) & 7) * 8;
+    float accs[4][4] = {};
+    mma_16xN<4>(accs, SMat{Qs, L, 1}, m0, SMat{Ks, 1, L}, nb, 0, D);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int r = acc_row(m0, e), c = acc_col(n0, e);
-      P[r * LP + c] = (c <= r && r < len) ? expf(G[r] - G[c]) * acc[e] : 0.f;
+    for (int b = 0; b < 4; ++b) {
+      const int n0 = nb + 8 * b;
+      float(&acc)[4] = accs[b];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = acc_row(m0, e), c = acc_col(n0, e);
+        P[r * LP + c] = (c <= r && r < len) ? expf(G[r] - G[c]) * acc[e] : 0.f;
+      }
     }
   }
   __syncthreads();
   // dV'_intra = scale P^T dO (this block's 64 value columns)
   float *out = reinterpret_cast<float *>(dvp.p);
-  for (int tl = warp * 4; tl < warp * 4 + 4; ++tl) {
-    const int m0 = (tl >> 3) * 16, n0 = (tl & 7) * 8;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    mma_16x8(acc, SMat{P, 1, LP}, m0, SMat{Ds, LP, 1}, n0, 0, 64);
+  {
+    const int m0 = ((warp * 4) >> 3) * 16, nb = ((warp * 4) & 7) * 8;
+    float accs[4][4] = {};
+    mma_16xN<4>(accs, SMat{P, 1, LP}, m0, SMat{Ds, LP, 1}, nb, 0, 64);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int r = acc_row(m0, e), c = acc_col(n0, e);
-      if (r < len) out[(t0 + r) * dvp.st + h * dvp.sh + cb + c] = scale * acc[e];
+    for (int b = 0; b < 4; ++b) {
+      const int n0 = nb + 8 * b;
+      float(&acc)[4] = accs[b];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = acc_row(m0, e), c = acc_col(n0, e);
+        if (r < len) out[(t0 + r) * dvp.st + h * dvp.sh + cb + c] = scale * acc[e];
+      }
     }
   }
 }
@@ -151,17 +161,22 @@ __global__ void __launch_bounds__(kScanCols * 4)
       Dos[(idx / kScanCols) * LC + idx % kScanCols] *= EG[idx / kScanCols];
     const int warp = tid >> 5;
     // dV' = dV'_intra + diag(e^{G_C - G}) K dS_C: 4 x CT tiles, four per warp
-    for (int tl = warp * 4; tl < warp * 4 + 4; ++tl) {
-      const int m0 = (tl / CT) * 16, n0 = (tl % CT) * 8;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_16x8(acc, SMat{Ks, LK, 1}, m0, SMat{dS, LC, 1}, n0, 0, D);
+    {
+      const int m0 = ((warp * 4) / CT) * 16, nb = ((warp * 4) % CT) * 8;
+      float accs[4][4] = {};
+      mma_16xN<4>(accs, SMat{Ks, LK, 1}, m0, SMat{dS, LC, 1}, nb, 0, D);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = acc_row(m0, e), j = acc_col(n0, e);
-        if (i < len) {
-          const float r = Vd[i * LC + j] + Dec[i] * acc[e];
-          Vd[i * LC + j] = r;
-          dvt[(t0 + i) * dvp.st + h * dvp.sh + jb + j] = r;
+      for (int b = 0; b < 4; ++b) {
+        const int n0 = nb + 8 * b;
+        float(&acc)[4] = accs[b];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = acc_row(m0, e), j = acc_col(n0, e);
+          if (i < len) {
+            const float r = Vd[i * LC + j] + Dec[i] * acc[e];
+            Vd[i * LC + j] = r;
+            dvt[(t0 + i) * dvp.st + h * dvp.sh + jb + j] = r;
+          }
         }
       }
     }
@@ -234,19 +249,26 @@ __global__ void __launch_bounds__(256)
   float *w_out = reinterpret_cast<float *>(dw.p);
   // 64 x kSRows outputs of each product: 32 tiles, four per warp
   const int warp = tid >> 5;
-  for (int tl = warp * 4; tl < warp * 4 + 4; ++tl) {
-    const int m0 = (tl >> 3) * 16, n0 = (tl & 7) * 8;
-    float aq[4] = {0.f, 0.f, 0.f, 0.f}, ak[4] = {0.f, 0.f, 0.f, 0.f}, aw[4] = {0.f, 0.f, 0.f, 0.f};
-    mma_16x8(aq, SMat{Dos, L, 1}, m0, SMat{S0, 1, L}, n0, 0, D);
-    mma_16x8(ak, SMat{Vp, L, 1}, m0, SMat{dS, 1, L}, n0, 0, D);
-    mma_16x8(aw, SMat{dV, L, 1}, m0, SMat{S0, 1, L}, n0, 0, D);
+  {
+    const int m0 = ((warp * 4) >> 3) * 16, nb = ((warp * 4) & 7) * 8;
+    float aqs[4][4] = {}, aks[4][4] = {}, aws[4][4] = {};
+    mma_16xN<4>(aqs, SMat{Dos, L, 1}, m0, SMat{S0, 1, L}, nb, 0, D);
+    mma_16xN<4>(aks, SMat{Vp, L, 1}, m0, SMat{dS, 1, L}, nb, 0, D);
+    mma_16xN<4>(aws, SMat{dV, L, 1}, m0, SMat{S0, 1, L}, nb, 0, D);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int i = acc_row(m0, e), r = acc_col(n0, e);
-      if (i < len) {
-        q_out[(t0 + i) * dqh.st + h * dqh.sh + rb + r] = scale * EG[i] * aq[e];
-        k_out[(t0 + i) * dkh.st + h * dkh.sh + rb + r] = Dec[i] * ak[e];
-        w_out[(t0 + i) * dw.st + h * dw.sh + rb + r] = -aw[e];
+    for (int b = 0; b < 4; ++b) {
+      const int n0 = nb + 8 * b;
+      float(&aq)[4] = aqs[b];
+      float(&ak)[4] = aks[b];
+      float(&aw)[4] = aws[b];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = acc_row(m0, e), r = acc_col(n0, e);
+        if (i < len) {
+          q_out[(t0 + i) * dqh.st + h * dqh.sh + rb + r] = scale * EG[i] * aq[e];
+          k_out[(t0 + i) * dkh.st + h * dkh.sh + rb + r] = Dec[i] * ak[e];
+          w_out[(t0 + i) * dw.st + h * dw.sh + rb + r] = -aw[e];
+        }
       }
     }
   }
@@ -313,17 +335,23 @@ __global__ void __launch_bounds__(256)
     }
   __syncthreads();
   // E_ij = scale (do_i . v'_j) Gam_ij and R_ij = E_ij (q_i . k_j), j <= i
-  for (int tl = warp * 4; tl < warp * 4 + 4; ++tl) {
-    const int m0 = (tl >> 3) * 16, n0 = (tl & 7) * 8;
-    float dv[4] = {0.f, 0.f, 0.f, 0.f}, qk[4] = {0.f, 0.f, 0.f, 0.f};
-    mma_16x8(dv, SMat{Dos, L, 1}, m0, SMat{Vp, 1, L}, n0, 0, D);
-    mma_16x8(qk, SMat{Qs, L, 1}, m0, SMat{Ks, 1, L}, n0, 0, D);
+  {
+    const int m0 = ((warp * 4) >> 3) * 16, nb = ((warp * 4) & 7) * 8;
+    float dvs[4][4] = {}, qks[4][4] = {};
+    mma_16xN<4>(dvs, SMat{Dos, L, 1}, m0, SMat{Vp, 1, L}, nb, 0, D);
+    mma_16xN<4>(qks, SMat{Qs, L, 1}, m0, SMat{Ks, 1, L}, nb, 0, D);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int i = acc_row(m0, e), j = acc_col(n0, e);
-      const float ev = (j <= i && i < len) ? scale * dv[e] * expf(G[i] - G[j]) : 0.f;
-      E[i * LE + j] = ev;
-      R[i * LE + j] = ev * qk[e];
+    for (int b = 0; b < 4; ++b) {
+      const int n0 = nb + 8 * b;
+      float(&dv)[4] = dvs[b];
+      float(&qk)[4] = qks[b];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = acc_row(m0, e), j = acc_col(n0, e);
+        const float ev = (j <= i && i < len) ? scale * dv[e] * expf(G[i] - G[j]) : 0.f;
+        E[i * LE + j] = ev;
+        R[i * LE + j] = ev * qk[e];
+      }
     }
   }
   __syncthreads();
@@ -439,51 +467,72 @@ __global__ void __launch_bounds__(256)
     BG[tid] = B[tid] * EGv[tid];
   }
   // raw key products k_i . k_j (j < i) and A_ij = beta_i Gam_ij k_i . k_j
-  for (int tl = warp * 4; tl < warp * 4 + 4; ++tl) {
-    const int m0 = (tl >> 3) * 16, n0 = (tl & 7) * 8;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    mma_16x8(acc, SMat{Ks, L, 1}, m0, SMat{Ks, 1, L}, n0, 0, D);
+  {
+    const int m0 = ((warp * 4) >> 3) * 16, nb = ((warp * 4) & 7) * 8;
+    float accs[4][4] = {};
+    mma_16xN<4>(accs, SMat{Ks, L, 1}, m0, SMat{Ks, 1, L}, nb, 0, D);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int i = acc_row(m0, e), j = acc_col(n0, e);
-      const bool lo = j < i && i < len;
-      KK[i * LK + j] = lo ? acc[e] : 0.f;
-      X[i * LT + j] = lo ? B[i] * expf(G[i] - G[j]) * acc[e] : 0.f;
+    for (int b = 0; b < 4; ++b) {
+      const int n0 = nb + 8 * b;
+      float(&acc)[4] = accs[b];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = acc_row(m0, e), j = acc_col(n0, e);
+        const bool lo = j < i && i < len;
+        KK[i * LK + j] = lo ? acc[e] : 0.f;
+        X[i * LT + j] = lo ? B[i] * expf(G[i] - G[j]) * acc[e] : 0.f;
+      }
     }
   }
   __syncthreads();
   solve_unit_lower64(X, LT, Tm, LT, dT);  // T = (I + A)^-1; dT's space as scratch until it is formed
   // dT_ij = beta_j (dU_i . v_j) + beta_j e^{G_j} (dW_i . k_j), i > j (the only part dA needs)
-  for (int tl = warp * 4; tl < warp * 4 + 4; ++tl) {
-    const int m0 = (tl >> 3) * 16, n0 = (tl & 7) * 8;
-    float du[4] = {0.f, 0.f, 0.f, 0.f}, dwk[4] = {0.f, 0.f, 0.f, 0.f};
-    mma_16x8(du, SMat{dVs, L, 1}, m0, SMat{Vs, 1, L}, n0, 0, D);
-    mma_16x8(dwk, SMat{dWs, L, 1}, m0, SMat{Ks, 1, L}, n0, 0, D);
+  {
+    const int m0 = ((warp * 4) >> 3) * 16, nb = ((warp * 4) & 7) * 8;
+    float dus[4][4] = {}, dwks[4][4] = {};
+    mma_16xN<4>(dus, SMat{dVs, L, 1}, m0, SMat{Vs, 1, L}, nb, 0, D);
+    mma_16xN<4>(dwks, SMat{dWs, L, 1}, m0, SMat{Ks, 1, L}, nb, 0, D);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int i = acc_row(m0, e), j = acc_col(n0, e);
-      dT[i * LT + j] = (j < i && i < len) ? B[j] * du[e] + BG[j] * dwk[e] : 0.f;
+    for (int b = 0; b < 4; ++b) {
+      const int n0 = nb + 8 * b;
+      float(&du)[4] = dus[b];
+      float(&dwk)[4] = dwks[b];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = acc_row(m0, e), j = acc_col(n0, e);
+        dT[i * LT + j] = (j < i && i < len) ? B[j] * du[e] + BG[j] * dwk[e] : 0.f;
+      }
     }
   }
   __syncthreads();
   // X = dT T^T
-  for (int tl = warp * 4; tl < warp * 4 + 4; ++tl) {
-    const int m0 = (tl >> 3) * 16, n0 = (tl & 7) * 8;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    mma_16x8(acc, SMat{dT, LT, 1}, m0, SMat{Tm, 1, LT}, n0, 0, 64);
+  {
+    const int m0 = ((warp * 4) >> 3) * 16, nb = ((warp * 4) & 7) * 8;
+    float accs[4][4] = {};
+    mma_16xN<4>(accs, SMat{dT, LT, 1}, m0, SMat{Tm, 1, LT}, nb, 0, 64);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) X[acc_row(m0, e) * LT + acc_col(n0, e)] = acc[e];
+    for (int b = 0; b < 4; ++b) {
+      const int n0 = nb + 8 * b;
+      float(&acc)[4] = accs[b];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) X[acc_row(m0, e) * LT + acc_col(n0, e)] = acc[e];
+    }
   }
   __syncthreads();
   // dA = -T^T X (i > j) into dT's place
-  for (int tl = warp * 4; tl < warp * 4 + 4; ++tl) {
-    const int m0 = (tl >> 3) * 16, n0 = (tl & 7) * 8;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    mma_16x8(acc, SMat{Tm, 1, LT}, m0, SMat{X, LT, 1}, n0, 0, 64);
+  {
+    const int m0 = ((warp * 4) >> 3) * 16, nb = ((warp * 4) & 7) * 8;
+    float accs[4][4] = {};
+    mma_16xN<4>(accs, SMat{Tm, 1, LT}, m0, SMat{X, LT, 1}, nb, 0, 64);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int i = acc_row(m0, e), j = acc_col(n0, e);
-      dT[i * LT + j] = (j < i && i < len) ? -acc[e] : 0.f;
+    for (int b = 0; b < 4; ++b) {
+      const int n0 = nb + 8 * b;
+      float(&acc)[4] = accs[b];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = acc_row(m0, e), j = acc_col(n0, e);
+        dT[i * LT + j] = (j < i && i < len) ? -acc[e] : 0.f;
+      }
     }
   }
   __syncthreads();

@@ -66,6 +66,32 @@ __device__ __forceinline__ void mma_16x8(float (&acc)[4], SMat A, int m0, SMat B
   }
 }
 
+// One warp: NB adjacent tiles, acc[b][16 x 8] += A[m0.., k] B[k, n0 + 8 b ..]; the A
+// fragment is loaded once per k step and the NB products are independent, so their
+// latencies overlap.
+template <int NB>
+__device__ __forceinline__ void mma_16xN(float (&acc)[NB][4], SMat A, int m0, SMat B, int n0,
+                                         int k0, int k1) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const float *ab = A.p + (m0 + g) * A.rs;
+#pragma unroll 2
+  for (int k = k0; k < k1; k += 8) {
+    const float *ap = ab + (k + t) * A.cs;
+    const uint32_t a0 = tf32_rn(ap[0]), a1 = tf32_rn(ap[8 * A.rs]);
+    const uint32_t a2 = tf32_rn(ap[4 * A.cs]), a3 = tf32_rn(ap[8 * A.rs + 4 * A.cs]);
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const float *bp = B.p + (n0 + 8 * b + g) * B.cs + (k + t) * B.rs;
+      const uint32_t b0 = tf32_rn(bp[0]), b1 = tf32_rn(bp[4 * B.rs]);
+      asm volatile(
+          "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+          "{%8,%9}, {%0,%1,%2,%3};"
+          : "+f"(acc[b][0]), "+f"(acc[b][1]), "+f"(acc[b][2]), "+f"(acc[b][3])
+          : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+  }
+}
+
 // Row and column of accumulator element e of this lane for the tile at (m0, n0).
 __device__ __forceinline__ int acc_row(int m0, int e) { return m0 + ((threadIdx.x & 31) >> 2) + 8 * (e >> 1); }
 __device__ __forceinline__ int acc_col(int n0, int e) { return n0 + 2 * (threadIdx.x & 3) + (e & 1); }

@@ -63,14 +63,19 @@ __global__ void __launch_bounds__(256)
   if (tid < 64) BG[tid] = B[tid] * expf(G[tid]);
   const int warp = tid >> 5;
   // A_ij = beta_i e^{G_i - G_j} k_i . k_j (j < i): 32 tiles of the key products
-  for (int tl = warp * 4; tl < warp * 4 + 4; ++tl) {
-    const int m0 = (tl >> 3) * 16, n0 = (tl & 7) * 8;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    mma_16x8(acc, SMat{Ks, L, 1}, m0, SMat{Ks, 1, L}, n0, 0, D);
+  {
+    const int m0 = ((warp * 4) >> 3) * 16, nb = ((warp * 4) & 7) * 8;
+    float accs[4][4] = {};
+    mma_16xN<4>(accs, SMat{Ks, L, 1}, m0, SMat{Ks, 1, L}, nb, 0, D);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int i = acc_row(m0, e), j = acc_col(n0, e);
-      Am[i * LA + j] = (j < i && i < len) ? B[i] * expf(G[i] - G[j]) * acc[e] : 0.f;
+    for (int b = 0; b < 4; ++b) {
+      const int n0 = nb + 8 * b;
+      float(&acc)[4] = accs[b];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = acc_row(m0, e), j = acc_col(n0, e);
+        Am[i * LA + j] = (j < i && i < len) ? B[i] * expf(G[i] - G[j]) * acc[e] : 0.f;
+      }
     }
   }
   __syncthreads();
@@ -165,20 +170,25 @@ __global__ void __launch_bounds__(kScanCols * 4)
     const int warp = tid >> 5;
     // V' = U - W S (bf16, as stored), and Vn = diag(e^{G_last - G}) V' for the update:
     // 64 x kScanCols outputs, four 16 x 8 tiles per warp on the tensor pipe
-    for (int tl = warp * 4; tl < warp * 4 + 4; ++tl) {
-      const int m0 = (tl / CT) * 16, n0 = (tl % CT) * 8;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_16x8(acc, SMat{Ws, LW, 1}, m0, SMat{S, LC, 1}, n0, 0, D);
+    {
+      const int m0 = ((warp * 4) / CT) * 16, nb = ((warp * 4) % CT) * 8;
+      float accs[4][4] = {};
+      mma_16xN<4>(accs, SMat{Ws, LW, 1}, m0, SMat{S, LC, 1}, nb, 0, D);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = acc_row(m0, e), j = acc_col(n0, e);
-        float vn = 0.f;
-        if (i < len) {
-          const __nv_bfloat16 b = __float2bfloat16_rn(Us[i * LC + j] - acc[e]);
-          reinterpret_cast<__nv_bfloat16 *>(v_new.p)[(t0 + i) * v_new.st + h * v_new.sh + jb + j] = b;
-          vn = Dec[i] * __bfloat162float(b);
+      for (int b = 0; b < 4; ++b) {
+        const int n0 = nb + 8 * b;
+        float(&acc)[4] = accs[b];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = acc_row(m0, e), j = acc_col(n0, e);
+          float vn = 0.f;
+          if (i < len) {
+            const __nv_bfloat16 b = __float2bfloat16_rn(Us[i * LC + j] - acc[e]);
+            reinterpret_cast<__nv_bfloat16 *>(v_new.p)[(t0 + i) * v_new.st + h * v_new.sh + jb + j] = b;
+            vn = Dec[i] * __bfloat162float(b);
+          }
+          Vn[i * LC + j] = vn;
         }
-        Vn[i * LC + j] = vn;
       }
     }
     __syncthreads();
