@@ -183,15 +183,24 @@ __global__ void __launch_bounds__(kScanCols * 4)
     __syncthreads();
     // dS_0 = e^{G_C} dS_C + scale Q^T diag(e^G) dO - W^T dV': D/16 x CT tiles
     const float eg = expf(glast);
-    for (int tl = warp; tl < (D / 16) * CT; tl += NW) {
-      const int m0 = (tl / CT) * 16, n0 = (tl % CT) * 8;
-      float inj[4] = {0.f, 0.f, 0.f, 0.f}, corr[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_16x8(inj, SMat{Qs, 1, LQ}, m0, SMat{Dos, LC, 1}, n0, 0, 64);
-      mma_16x8(corr, SMat{Ws, 1, LQ}, m0, SMat{Vd, LC, 1}, n0, 0, 64);
+    static_assert(NW == CT, "one column tile per warp");
+    {
+      // warp w: every row tile of column tile w, in two halves (fewer live accumulators)
+      const int n0 = warp * 8;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int d = acc_row(m0, e), j = acc_col(n0, e);
-        dS[d * LC + j] = eg * dS[d * LC + j] + scale * inj[e] - corr[e];
+      for (int half = 0; half < 2; ++half) {
+        constexpr int MB = D / 32;
+        const int m0 = half * (D / 2);
+        float inj[MB][4] = {}, corr[MB][4] = {};
+        mma_Mx8<MB>(inj, SMat{Qs, 1, LQ}, m0, SMat{Dos, LC, 1}, n0, 0, 64);
+        mma_Mx8<MB>(corr, SMat{Ws, 1, LQ}, m0, SMat{Vd, LC, 1}, n0, 0, 64);
+#pragma unroll
+        for (int r = 0; r < MB; ++r)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int d = acc_row(m0 + 16 * r, e), j = acc_col(n0, e);
+            dS[d * LC + j] = eg * dS[d * LC + j] + scale * inj[r][e] - corr[r][e];
+          }
       }
     }
   }

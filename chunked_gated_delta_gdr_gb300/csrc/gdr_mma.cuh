@@ -92,6 +92,31 @@ __device__ __forceinline__ void mma_16xN(float (&acc)[NB][4], SMat A, int m0, SM
   }
 }
 
+// One warp: MB row tiles (m0 + 16 r) sharing one column tile (n0); the B fragment is
+// loaded once per k step and the MB products are independent.
+template <int MB>
+__device__ __forceinline__ void mma_Mx8(float (&acc)[MB][4], SMat A, int m0, SMat B, int n0,
+                                        int k0, int k1) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const float *bb = B.p + (n0 + g) * B.cs;
+#pragma unroll 2
+  for (int k = k0; k < k1; k += 8) {
+    const float *bp = bb + (k + t) * B.rs;
+    const uint32_t b0 = tf32_rn(bp[0]), b1 = tf32_rn(bp[4 * B.rs]);
+#pragma unroll
+    for (int r = 0; r < MB; ++r) {
+      const float *ap = A.p + (m0 + 16 * r + g) * A.rs + (k + t) * A.cs;
+      const uint32_t a0 = tf32_rn(ap[0]), a1 = tf32_rn(ap[8 * A.rs]);
+      const uint32_t a2 = tf32_rn(ap[4 * A.cs]), a3 = tf32_rn(ap[8 * A.rs + 4 * A.cs]);
+      asm volatile(
+          "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+          "{%8,%9}, {%0,%1,%2,%3};"
+          : "+f"(acc[r][0]), "+f"(acc[r][1]), "+f"(acc[r][2]), "+f"(acc[r][3])
+          : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+  }
+}
+
 // Row and column of accumulator element e of this lane for the tile at (m0, n0).
 __device__ __forceinline__ int acc_row(int m0, int e) { return m0 + ((threadIdx.x & 31) >> 2) + 8 * (e >> 1); }
 __device__ __forceinline__ int acc_col(int n0, int e) { return n0 + 2 * (threadIdx.x & 3) + (e & 1); }

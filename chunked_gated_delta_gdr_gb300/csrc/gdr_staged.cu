@@ -194,15 +194,20 @@ __global__ void __launch_bounds__(kScanCols * 4)
     __syncthreads();
     // S <- e^{G_last} S + K^T Vn: D x kScanCols outputs
     const float eg = expf(glast);
-    for (int tl = warp; tl < (D / 16) * CT; tl += NW) {
-      const int m0 = (tl / CT) * 16, n0 = (tl % CT) * 8;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_16x8(acc, SMat{Ks, 1, LK}, m0, SMat{Vn, LC, 1}, n0, 0, 64);
+    static_assert(NW == CT, "one column tile per warp");
+    {
+      // warp w: every row tile of column tile w
+      constexpr int MB = D / 16;
+      const int n0 = warp * 8;
+      float acc[MB][4] = {};
+      mma_Mx8<MB>(acc, SMat{Ks, 1, LK}, 0, SMat{Vn, LC, 1}, n0, 0, 64);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int d = acc_row(m0, e), j = acc_col(n0, e);
-        S[d * LC + j] = eg * S[d * LC + j] + acc[e];
-      }
+      for (int r = 0; r < MB; ++r)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int d = acc_row(16 * r, e), j = acc_col(n0, e);
+          S[d * LC + j] = eg * S[d * LC + j] + acc[r][e];
+        }
     }
   }
   if (ht || ck.h) __syncthreads();
