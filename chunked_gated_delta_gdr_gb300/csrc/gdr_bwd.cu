@@ -49,7 +49,7 @@ struct DvIntraSmem {
 };
 
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kChunkThreads)
     k_bwd_dv_intra(int32_t group, View q, View k, View dout, View gcum, float scale, View dvp,
                    const ChunkInfo *__restrict__ chunks, const int32_t *__restrict__ n_chunks,
                    bool vec) {
@@ -61,19 +61,19 @@ __global__ void __launch_bounds__(256)
   const int len = ci.len, hk = h / group;
   const int64_t t0 = ci.start;
   float *Qs = sm, *Ks = Qs + 64 * L, *Ds = Ks + 64 * L, *P = Ds + 64 * LP, *G = P + 64 * LP;
-  tile_bf16<64, D, 256>(Qs, L, bf_row(q, t0, hk), q.st, len, vec);
-  tile_bf16<64, D, 256>(Ks, L, bf_row(k, t0, hk), k.st, len, vec);
-  tile_bf16<64, 64, 256>(Ds, LP, bf_row(dout, t0, h) + cb, dout.st, len, vec);
+  tile_bf16<64, D, kChunkThreads>(Qs, L, bf_row(q, t0, hk), q.st, len, vec);
+  tile_bf16<64, D, kChunkThreads>(Ks, L, bf_row(k, t0, hk), k.st, len, vec);
+  tile_bf16<64, 64, kChunkThreads>(Ds, LP, bf_row(dout, t0, h) + cb, dout.st, len, vec);
   if (tid < 64) G[tid] = tid < len ? ldf(gcum.p, (t0 + tid) * gcum.st + h * gcum.sh) : 0.f;
   __syncthreads();
   const int warp = tid >> 5;
   // P = (Q K^T) o Gam (j <= i): 32 tiles of 16 x 8, four per warp
   {
-    const int m0 = ((warp * 4) >> 3) * 16, nb = ((warp * 4) & 7) * 8;
-    float accs[4][4] = {};
-    mma_16xN<4>(accs, SMat{Qs, L, 1}, m0, SMat{Ks, 1, L}, nb, 0, D);
+    const int m0 = ((warp * kTPW) >> 3) * 16, nb = ((warp * kTPW) & 7) * 8;
+    float accs[kTPW][4] = {};
+    mma_16xN<kTPW>(accs, SMat{Qs, L, 1}, m0, SMat{Ks, 1, L}, nb, 0, D);
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
+    for (int b = 0; b < kTPW; ++b) {
       const int n0 = nb + 8 * b;
       float(&acc)[4] = accs[b];
 #pragma unroll
@@ -87,11 +87,11 @@ __global__ void __launch_bounds__(256)
   // dV'_intra = scale P^T dO (this block's 64 value columns)
   float *out = reinterpret_cast<float *>(dvp.p);
   {
-    const int m0 = ((warp * 4) >> 3) * 16, nb = ((warp * 4) & 7) * 8;
-    float accs[4][4] = {};
-    mma_16xN<4>(accs, SMat{P, 1, LP}, m0, SMat{Ds, LP, 1}, nb, 0, 64);
+    const int m0 = ((warp * kTPW) >> 3) * 16, nb = ((warp * kTPW) & 7) * 8;
+    float accs[kTPW][4] = {};
+    mma_16xN<kTPW>(accs, SMat{P, 1, LP}, m0, SMat{Ds, LP, 1}, nb, 0, 64);
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
+    for (int b = 0; b < kTPW; ++b) {
       const int n0 = nb + 8 * b;
       float(&acc)[4] = accs[b];
 #pragma unroll
@@ -220,11 +220,11 @@ template <int D>
 struct SgradSmem {
   static constexpr int kLd = ld_rows(D);
   static constexpr size_t bytes =
-      sizeof(float) * (2 * kSRows * kLd + 3 * 64 * kLd + 2 * 64 + 256);
+      sizeof(float) * (2 * kSRows * kLd + 3 * 64 * kLd + 2 * 64 + kChunkThreads);
 };
 
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kChunkThreads)
     k_bwd_sgrad(View dout, View v_new, View gcum, float scale, const __nv_bfloat16 *hbuf,
                 const float *dh, View dvp, View dqh, View dkh, View dw, float *sdot,
                 const ChunkInfo *__restrict__ chunks, const int32_t *__restrict__ n_chunks,
@@ -240,13 +240,13 @@ __global__ void __launch_bounds__(256)
   float *dV = Vp + 64 * L, *Dec = dV + 64 * L, *EG = Dec + 64, *red = EG + 64;
   const __nv_bfloat16 *hc = hbuf + ((int64_t)cid * H + h) * D * D;
   const float *dhc = dh + ((int64_t)cid * H + h) * D * D;
-  tile_bf16<kSRows, D, 256>(S0, L, hc + (int64_t)rb * D, D, kSRows, true);
-  tile_f32<kSRows, D, 256>(dS, L, dhc + (int64_t)rb * D, D, kSRows);
+  tile_bf16<kSRows, D, kChunkThreads>(S0, L, hc + (int64_t)rb * D, D, kSRows, true);
+  tile_f32<kSRows, D, kChunkThreads>(dS, L, dhc + (int64_t)rb * D, D, kSRows);
   const float *dvt = reinterpret_cast<const float *>(dvp.p);
-  tile_bf16<64, D, 256>(Dos, L, bf_row(dout, t0, h), dout.st, len, vec);
-  tile_bf16<64, D, 256>(Vp, L, bf_row(v_new, t0, h), v_new.st, len,
+  tile_bf16<64, D, kChunkThreads>(Dos, L, bf_row(dout, t0, h), dout.st, len, vec);
+  tile_bf16<64, D, kChunkThreads>(Vp, L, bf_row(v_new, t0, h), v_new.st, len,
                         true);
-  tile_f32<64, D, 256>(dV, L, dvt + t0 * dvp.st + h * dvp.sh, dvp.st, len);
+  tile_f32<64, D, kChunkThreads>(dV, L, dvt + t0 * dvp.st + h * dvp.sh, dvp.st, len);
   if (tid < 64) {
     const float gi = tid < len ? ldf(gcum.p, (t0 + tid) * gcum.st + h * gcum.sh) : 0.f;
     const float gl = ldf(gcum.p, (t0 + len - 1) * gcum.st + h * gcum.sh);
@@ -259,13 +259,13 @@ __global__ void __launch_bounds__(256)
   // 64 x kSRows outputs of each product: 32 tiles, four per warp
   const int warp = tid >> 5;
   {
-    const int m0 = ((warp * 4) >> 3) * 16, nb = ((warp * 4) & 7) * 8;
-    float aqs[4][4] = {}, aks[4][4] = {}, aws[4][4] = {};
-    mma_16xN<4>(aqs, SMat{Dos, L, 1}, m0, SMat{S0, 1, L}, nb, 0, D);
-    mma_16xN<4>(aks, SMat{Vp, L, 1}, m0, SMat{dS, 1, L}, nb, 0, D);
-    mma_16xN<4>(aws, SMat{dV, L, 1}, m0, SMat{S0, 1, L}, nb, 0, D);
+    const int m0 = ((warp * kTPW) >> 3) * 16, nb = ((warp * kTPW) & 7) * 8;
+    float aqs[kTPW][4] = {}, aks[kTPW][4] = {}, aws[kTPW][4] = {};
+    mma_16xN<kTPW>(aqs, SMat{Dos, L, 1}, m0, SMat{S0, 1, L}, nb, 0, D);
+    mma_16xN<kTPW>(aks, SMat{Vp, L, 1}, m0, SMat{dS, 1, L}, nb, 0, D);
+    mma_16xN<kTPW>(aws, SMat{dV, L, 1}, m0, SMat{S0, 1, L}, nb, 0, D);
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
+    for (int b = 0; b < kTPW; ++b) {
       const int n0 = nb + 8 * b;
       float(&aq)[4] = aqs[b];
       float(&ak)[4] = aks[b];
@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(256)
   }
   red[tid] = part;
   __syncthreads();
-  for (int s = 128; s > 0; s >>= 1) {
+  for (int s = kChunkThreads / 2; s > 0; s >>= 1) {
     if (tid < s) red[tid] += red[tid + s];
     __syncthreads();
   }
@@ -300,14 +300,14 @@ __global__ void __launch_bounds__(256)
 template <int D>
 struct IntraSmem {
   static constexpr int kLd = ld_rows(D), kLdE = ld_rows(64);
-  static constexpr size_t bytes = sizeof(float) * (4 * 64 * kLd + 2 * 64 * kLdE + 7 * 64);
+  static constexpr size_t bytes = sizeof(float) * (4 * 64 * kLd + 2 * 64 * kLdE + (3 + 2 * kQ) * 64);
 };
 
-// Warp w owns rows 16 (w % 4) .. +16 and half of the D columns (w / 4) of the 64 x D
-// products; row sums go through a shuffle inside the tile, then two per-warp partials
+// Warp w owns rows 16 (w % 4) .. +16 and column group w / 4 (of kQ) of the 64 x D
+// products; row sums go through a shuffle inside the tile, then kQ per-warp partials
 // added in a fixed order.
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kChunkThreads)
     k_bwd_intra(int32_t group, View q, View k, View dout, View v_new, View gcum, float scale,
                 View dqh, View dkh, float *dga, const ChunkInfo *__restrict__ chunks,
                 const int32_t *__restrict__ n_chunks, int32_t H, bool vec) {
@@ -320,37 +320,37 @@ __global__ void __launch_bounds__(256)
   const int64_t t0 = ci.start;
   float *Qs = sm, *Ks = Qs + 64 * L, *Dos = Ks + 64 * L, *Vp = Dos + 64 * L;
   float *E = Vp + 64 * L, *R = E + 64 * LE, *G = R + 64 * LE, *rowR = G + 64, *colR = rowR + 64;
-  float *aP = colR + 64, *cP = aP + 128;  // [2][64] partial row sums
-  tile_bf16<64, D, 256>(Qs, L, bf_row(q, t0, hk), q.st, len, vec);
-  tile_bf16<64, D, 256>(Ks, L, bf_row(k, t0, hk), k.st, len, vec);
-  tile_bf16<64, D, 256>(Dos, L, bf_row(dout, t0, h), dout.st, len, vec);
-  tile_bf16<64, D, 256>(Vp, L, bf_row(v_new, t0, h), v_new.st, len,
+  float *aP = colR + 64, *cP = aP + kQ * 64;  // [kQ][64] partial row sums
+  tile_bf16<64, D, kChunkThreads>(Qs, L, bf_row(q, t0, hk), q.st, len, vec);
+  tile_bf16<64, D, kChunkThreads>(Ks, L, bf_row(k, t0, hk), k.st, len, vec);
+  tile_bf16<64, D, kChunkThreads>(Dos, L, bf_row(dout, t0, h), dout.st, len, vec);
+  tile_bf16<64, D, kChunkThreads>(Vp, L, bf_row(v_new, t0, h), v_new.st, len,
                         true);
   if (tid < 64) G[tid] = tid < len ? ldf(gcum.p, (t0 + tid) * gcum.st + h * gcum.sh) : 0.f;
   const int warp = tid >> 5;
   // this thread's elements of the dQ / dK accumulators (written by k_bwd_sgrad), loaded
   // now so that the loads overlap the products below
   float *q_out = reinterpret_cast<float *>(dqh.p), *k_out = reinterpret_cast<float *>(dkh.p);
-  const int m0 = (warp & 3) * 16, half = warp >> 2;
-  constexpr int kCT = D / 16;  // column tiles per warp
+  const int m0 = (warp & 3) * 16, cg = warp >> 2;
+  constexpr int kCT = D / (8 * kQ);  // column tiles per warp
   float qpre[kCT][4], kpre[kCT][4];
 #pragma unroll
   for (int c = 0; c < kCT; ++c)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const int i = acc_row(m0, e), d = acc_col((half * kCT + c) * 8, e);
+      const int i = acc_row(m0, e), d = acc_col((cg * kCT + c) * 8, e);
       qpre[c][e] = i < len ? q_out[(t0 + i) * dqh.st + h * dqh.sh + d] : 0.f;
       kpre[c][e] = i < len ? k_out[(t0 + i) * dkh.st + h * dkh.sh + d] : 0.f;
     }
   __syncthreads();
   // E_ij = scale (do_i . v'_j) Gam_ij and R_ij = E_ij (q_i . k_j), j <= i
   {
-    const int m0 = ((warp * 4) >> 3) * 16, nb = ((warp * 4) & 7) * 8;
-    float dvs[4][4] = {}, qks[4][4] = {};
-    mma_16xN<4>(dvs, SMat{Dos, L, 1}, m0, SMat{Vp, 1, L}, nb, 0, D);
-    mma_16xN<4>(qks, SMat{Qs, L, 1}, m0, SMat{Ks, 1, L}, nb, 0, D);
+    const int m0 = ((warp * kTPW) >> 3) * 16, nb = ((warp * kTPW) & 7) * 8;
+    float dvs[kTPW][4] = {}, qks[kTPW][4] = {};
+    mma_16xN<kTPW>(dvs, SMat{Dos, L, 1}, m0, SMat{Vp, 1, L}, nb, 0, D);
+    mma_16xN<kTPW>(qks, SMat{Qs, L, 1}, m0, SMat{Ks, 1, L}, nb, 0, D);
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
+    for (int b = 0; b < kTPW; ++b) {
       const int n0 = nb + 8 * b;
       float(&dv)[4] = dvs[b];
       float(&qk)[4] = qks[b];
@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(256)
   float ap[2] = {0.f, 0.f}, cp[2] = {0.f, 0.f};
 #pragma unroll
   for (int c = 0; c < kCT; ++c) {
-    const int n0 = (half * kCT + c) * 8;
+    const int n0 = (cg * kCT + c) * 8;
     float dq[4] = {0.f, 0.f, 0.f, 0.f}, dk[4] = {0.f, 0.f, 0.f, 0.f};
     mma_16x8(dq, SMat{E, LE, 1}, m0, SMat{Ks, L, 1}, n0, 0, 64);
     mma_16x8(dk, SMat{E, 1, LE}, m0, SMat{Qs, L, 1}, n0, 0, 64);
@@ -402,20 +402,25 @@ __global__ void __launch_bounds__(256)
   }
   if ((tid & 3) == 0) {
     const int r0 = m0 + ((tid & 31) >> 2);
-    aP[half * 64 + r0] = ap[0];
-    aP[half * 64 + r0 + 8] = ap[1];
-    cP[half * 64 + r0] = cp[0];
-    cP[half * 64 + r0 + 8] = cp[1];
+    aP[cg * 64 + r0] = ap[0];
+    aP[cg * 64 + r0 + 8] = ap[1];
+    cP[cg * 64 + r0] = cp[0];
+    cP[cg * 64 + r0 + 8] = cp[1];
   }
   __syncthreads();
   // dG from the output (e^G on S_0, Gam) and from the state's e^{G_C - G_i} factors;
   // the e^{G_C} S_0 term is added by k_bwd_wy
   if (tid < len) {
-    const float c_t = cP[tid] + cP[64 + tid];
-    float v = (aP[tid] + aP[64 + tid]) - c_t + rowR[tid] - colR[tid];
+    float a_t = 0.f, c_t = 0.f;
+    for (int q = 0; q < kQ; ++q) {
+      a_t += aP[q * 64 + tid];
+      c_t += cP[q * 64 + tid];
+    }
+    float v = a_t - c_t + rowR[tid] - colR[tid];
     if (tid == len - 1) {
       float sc = 0.f;
-      for (int r = 0; r < len; ++r) sc += cP[r] + cP[64 + r];
+      for (int r = 0; r < len; ++r)
+        for (int q = 0; q < kQ; ++q) sc += cP[q * 64 + r];
       v += sc;
     }
     dga[(t0 + tid) * H + h] = v;
@@ -427,11 +432,11 @@ template <int D>
 struct WySmem {
   static constexpr int kLd = ld_rows(D), kLdK = ld_rows(64), kLdT = ld_cols(64);
   static constexpr size_t bytes =
-      sizeof(float) * (4 * 64 * kLd + 64 * kLdK + 3 * 64 * kLdT + 11 * 64);
+      sizeof(float) * (4 * 64 * kLd + 64 * kLdK + 3 * 64 * kLdT + (5 + 4 * kQ) * 64);
 };
 
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kChunkThreads)
     k_bwd_wy(int32_t group, View k, View v, View beta, View gcum, View dvp, View dw, View dkh,
              const float *dga, const float *sdot, View dv_out, View dbeta_out, View dg_out,
              const ChunkInfo *__restrict__ chunks, const int32_t *__restrict__ n_chunks,
@@ -446,12 +451,12 @@ __global__ void __launch_bounds__(256)
   float *Ks = sm, *Vs = Ks + 64 * L, *dVs = Vs + 64 * L, *dWs = dVs + 64 * L;
   float *KK = dWs + 64 * L, *Tm = KK + 64 * LK, *dT = Tm + 64 * LT, *X = dT + 64 * LT;
   float *G = X + 64 * LT, *B = G + 64, *BG = B + 64, *EGv = BG + 64, *dGt = EGv + 64;
-  float *baP = dGt + 64, *bbP = baP + 128;  // [2][64] partial row sums
+  float *baP = dGt + 64, *bbP = baP + kQ * 64;  // [kQ][64] partial row sums
   const float *dvt = reinterpret_cast<const float *>(dvp.p), *dwt = reinterpret_cast<const float *>(dw.p);
-  tile_bf16<64, D, 256>(Ks, L, bf_row(k, t0, hk), k.st, len, vec);
-  tile_bf16<64, D, 256>(Vs, L, bf_row(v, t0, h), v.st, len, vec);
-  tile_f32<64, D, 256>(dVs, L, dvt + t0 * dvp.st + h * dvp.sh, dvp.st, len);
-  tile_f32<64, D, 256>(dWs, L, dwt + t0 * dw.st + h * dw.sh, dw.st, len);
+  tile_bf16<64, D, kChunkThreads>(Ks, L, bf_row(k, t0, hk), k.st, len, vec);
+  tile_bf16<64, D, kChunkThreads>(Vs, L, bf_row(v, t0, h), v.st, len, vec);
+  tile_f32<64, D, kChunkThreads>(dVs, L, dvt + t0 * dvp.st + h * dvp.sh, dvp.st, len);
+  tile_f32<64, D, kChunkThreads>(dWs, L, dwt + t0 * dw.st + h * dw.sh, dw.st, len);
   if (tid < 64) {
     const bool in = tid < len;
     G[tid] = in ? ldf(gcum.p, (t0 + tid) * gcum.st + h * gcum.sh) : 0.f;
@@ -460,14 +465,14 @@ __global__ void __launch_bounds__(256)
   const int warp = tid >> 5;
   // this thread's elements of the dK accumulator, loaded early (used at the end)
   float *dvo = reinterpret_cast<float *>(dv_out.p), *dko = reinterpret_cast<float *>(dkh.p);
-  const int m0 = (warp & 3) * 16, half = warp >> 2;
-  constexpr int kCT = D / 16;
+  const int m0 = (warp & 3) * 16, cg = warp >> 2;
+  constexpr int kCT = D / (8 * kQ);
   float kpre[kCT][4];
 #pragma unroll
   for (int c = 0; c < kCT; ++c)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const int j = acc_row(m0, e), d = acc_col((half * kCT + c) * 8, e);
+      const int j = acc_row(m0, e), d = acc_col((cg * kCT + c) * 8, e);
       kpre[c][e] = j < len ? dko[(t0 + j) * dkh.st + h * dkh.sh + d] : 0.f;
     }
   __syncthreads();
@@ -477,11 +482,11 @@ __global__ void __launch_bounds__(256)
   }
   // raw key products k_i . k_j (j < i) and A_ij = beta_i Gam_ij k_i . k_j
   {
-    const int m0 = ((warp * 4) >> 3) * 16, nb = ((warp * 4) & 7) * 8;
-    float accs[4][4] = {};
-    mma_16xN<4>(accs, SMat{Ks, L, 1}, m0, SMat{Ks, 1, L}, nb, 0, D);
+    const int m0 = ((warp * kTPW) >> 3) * 16, nb = ((warp * kTPW) & 7) * 8;
+    float accs[kTPW][4] = {};
+    mma_16xN<kTPW>(accs, SMat{Ks, L, 1}, m0, SMat{Ks, 1, L}, nb, 0, D);
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
+    for (int b = 0; b < kTPW; ++b) {
       const int n0 = nb + 8 * b;
       float(&acc)[4] = accs[b];
 #pragma unroll
@@ -497,12 +502,12 @@ __global__ void __launch_bounds__(256)
   solve_unit_lower64(X, LT, Tm, LT, dT);  // T = (I + A)^-1; dT's space as scratch until it is formed
   // dT_ij = beta_j (dU_i . v_j) + beta_j e^{G_j} (dW_i . k_j), i > j (the only part dA needs)
   {
-    const int m0 = ((warp * 4) >> 3) * 16, nb = ((warp * 4) & 7) * 8;
-    float dus[4][4] = {}, dwks[4][4] = {};
-    mma_16xN<4>(dus, SMat{dVs, L, 1}, m0, SMat{Vs, 1, L}, nb, 0, D);
-    mma_16xN<4>(dwks, SMat{dWs, L, 1}, m0, SMat{Ks, 1, L}, nb, 0, D);
+    const int m0 = ((warp * kTPW) >> 3) * 16, nb = ((warp * kTPW) & 7) * 8;
+    float dus[kTPW][4] = {}, dwks[kTPW][4] = {};
+    mma_16xN<kTPW>(dus, SMat{dVs, L, 1}, m0, SMat{Vs, 1, L}, nb, 0, D);
+    mma_16xN<kTPW>(dwks, SMat{dWs, L, 1}, m0, SMat{Ks, 1, L}, nb, 0, D);
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
+    for (int b = 0; b < kTPW; ++b) {
       const int n0 = nb + 8 * b;
       float(&du)[4] = dus[b];
       float(&dwk)[4] = dwks[b];
@@ -516,11 +521,11 @@ __global__ void __launch_bounds__(256)
   __syncthreads();
   // X = dT T^T
   {
-    const int m0 = ((warp * 4) >> 3) * 16, nb = ((warp * 4) & 7) * 8;
-    float accs[4][4] = {};
-    mma_16xN<4>(accs, SMat{dT, LT, 1}, m0, SMat{Tm, 1, LT}, nb, 0, 64);
+    const int m0 = ((warp * kTPW) >> 3) * 16, nb = ((warp * kTPW) & 7) * 8;
+    float accs[kTPW][4] = {};
+    mma_16xN<kTPW>(accs, SMat{dT, LT, 1}, m0, SMat{Tm, 1, LT}, nb, 0, 64);
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
+    for (int b = 0; b < kTPW; ++b) {
       const int n0 = nb + 8 * b;
       float(&acc)[4] = accs[b];
 #pragma unroll
@@ -530,11 +535,11 @@ __global__ void __launch_bounds__(256)
   __syncthreads();
   // dA = -T^T X (i > j) into dT's place
   {
-    const int m0 = ((warp * 4) >> 3) * 16, nb = ((warp * 4) & 7) * 8;
-    float accs[4][4] = {};
-    mma_16xN<4>(accs, SMat{Tm, 1, LT}, m0, SMat{X, LT, 1}, nb, 0, 64);
+    const int m0 = ((warp * kTPW) >> 3) * 16, nb = ((warp * kTPW) & 7) * 8;
+    float accs[kTPW][4] = {};
+    mma_16xN<kTPW>(accs, SMat{Tm, 1, LT}, m0, SMat{X, LT, 1}, nb, 0, 64);
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
+    for (int b = 0; b < kTPW; ++b) {
       const int n0 = nb + 8 * b;
       float(&acc)[4] = accs[b];
 #pragma unroll
@@ -551,11 +556,12 @@ __global__ void __launch_bounds__(256)
     X[i * LT + j] = (j < i && i < len) ? dT[i * LT + j] * B[i] * expf(G[i] - G[j]) : 0.f;
   }
   __syncthreads();
-  // per row j: T^T dU, T^T dW, (B + B^T) K; warp w owns rows 16 (w % 4) .. +16, half the columns
+  // per row j: T^T dU, T^T dW, (B + B^T) K; warp w owns rows 16 (w % 4) .. +16 and column
+  // group w / 4
   float ba[2] = {0.f, 0.f}, bb[2] = {0.f, 0.f};
 #pragma unroll
   for (int c = 0; c < kCT; ++c) {
-    const int n0 = (half * kCT + c) * 8;
+    const int n0 = (cg * kCT + c) * 8;
     float tdu[4] = {0.f, 0.f, 0.f, 0.f}, tdw[4] = {0.f, 0.f, 0.f, 0.f}, kc[4] = {0.f, 0.f, 0.f, 0.f};
     mma_16x8(tdu, SMat{Tm, 1, LT}, m0, SMat{dVs, L, 1}, n0, 0, 64);
     mma_16x8(tdw, SMat{Tm, 1, LT}, m0, SMat{dWs, L, 1}, n0, 0, 64);
@@ -581,10 +587,10 @@ __global__ void __launch_bounds__(256)
   }
   if ((tid & 3) == 0) {
     const int r0 = m0 + ((tid & 31) >> 2);
-    baP[half * 64 + r0] = ba[0];
-    baP[half * 64 + r0 + 8] = ba[1];
-    bbP[half * 64 + r0] = bb[0];
-    bbP[half * 64 + r0 + 8] = bb[1];
+    baP[cg * 64 + r0] = ba[0];
+    baP[cg * 64 + r0 + 8] = ba[1];
+    bbP[cg * 64 + r0] = bb[0];
+    bbP[cg * 64 + r0 + 8] = bb[1];
   }
   __syncthreads();
   if (tid < 64) {
@@ -596,7 +602,11 @@ __global__ void __launch_bounds__(256)
         rowq += X[r * LT + x] * KK[r * LK + x];
       }
       for (int a = r + 1; a < len; ++a) colq += X[a * LT + r] * KK[a * LK + r];
-      const float dba = baP[r] + baP[64 + r], dbb = bbP[r] + bbP[64 + r];
+      float dba = 0.f, dbb = 0.f;
+      for (int q = 0; q < kQ; ++q) {
+        dba += baP[q * 64 + r];
+        dbb += bbP[q * 64 + r];
+      }
       float *dbo = reinterpret_cast<float *>(dbeta_out.p);
       dbo[(t0 + r) * dbeta_out.st + h * dbeta_out.sh] = dba + EGv[r] * dbb + dbc;
       float gt = dga[(t0 + r) * H + h] + BG[r] * dbb + rowq - colq;
@@ -706,7 +716,7 @@ cudaError_t launch_bwd_d(const BwdArgs &a, const BwdWs &w, cudaStream_t stream) 
     return e;
   const dim3 gc((unsigned)s.chunk_cap, (unsigned)s.H);
   if ((e = set_smem(k_bwd_dv_intra<D>, DvIntraSmem<D>::bytes)) != cudaSuccess) return e;
-  k_bwd_dv_intra<D><<<dim3(gc.x, gc.y, D / 64), 256, DvIntraSmem<D>::bytes, stream>>>(
+  k_bwd_dv_intra<D><<<dim3(gc.x, gc.y, D / 64), kChunkThreads, DvIntraSmem<D>::bytes, stream>>>(
       group, a.q, a.k, a.dout, vg, a.scale, vdvp, a.chunks, a.n_chunks, vec);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   auto scan = [&](auto kern, int cols, size_t bytes) -> cudaError_t {
@@ -720,17 +730,17 @@ cudaError_t launch_bwd_d(const BwdArgs &a, const BwdWs &w, cudaStream_t stream) 
                                        : scan(k_bwd_scan<D, 32>, 32, BwdScanSmem<D, 32>::bytes);
   if (e != cudaSuccess) return e;
   if ((e = set_smem(k_bwd_sgrad<D>, SgradSmem<D>::bytes)) != cudaSuccess) return e;
-  k_bwd_sgrad<D><<<dim3(gc.x, gc.y, D / kSRows), 256, SgradSmem<D>::bytes, stream>>>(
+  k_bwd_sgrad<D><<<dim3(gc.x, gc.y, D / kSRows), kChunkThreads, SgradSmem<D>::bytes, stream>>>(
       a.dout, vn, vg, a.scale, reinterpret_cast<const __nv_bfloat16 *>(w.h), w.dh, vdvp, vdqh,
       vdkh, vdw, w.sdot, a.chunks, a.n_chunks, s.H, vec);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = set_smem(k_bwd_intra<D>, IntraSmem<D>::bytes)) != cudaSuccess) return e;
-  k_bwd_intra<D><<<gc, 256, IntraSmem<D>::bytes, stream>>>(group, a.q, a.k, a.dout, vn, vg,
+  k_bwd_intra<D><<<gc, kChunkThreads, IntraSmem<D>::bytes, stream>>>(group, a.q, a.k, a.dout, vn, vg,
                                                             a.scale, vdqh, vdkh, w.dga,
                                                             a.chunks, a.n_chunks, s.H, vec);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = set_smem(k_bwd_wy<D>, WySmem<D>::bytes)) != cudaSuccess) return e;
-  k_bwd_wy<D><<<gc, 256, WySmem<D>::bytes, stream>>>(group, a.k, a.v, a.beta, vg, vdvp, vdw,
+  k_bwd_wy<D><<<gc, kChunkThreads, WySmem<D>::bytes, stream>>>(group, a.k, a.v, a.beta, vg, vdvp, vdw,
                                                       vdkh, w.dga, w.sdot, a.dv, a.dbeta, a.dg,
                                                       a.chunks, a.n_chunks, s.H, vec);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -120,6 +120,12 @@ __device__ __forceinline__ void mma_Mx8(float (&acc)[MB][4], SMat A, int m0, SMa
 __device__ __forceinline__ int acc_row(int m0, int e) { return m0 + ((threadIdx.x & 31) >> 2) + 8 * (e >> 1); }
 __device__ __forceinline__ int acc_col(int n0, int e) { return n0 + 2 * (threadIdx.x & 3) + (e & 1); }
 
+// Threads of the per-chunk kernels (one block per chunk and head): 16 warps; a 64 x 64
+// tile matrix is 32 MMA tiles of 16 x 8, kTPW per warp; in phases where warps own
+// row tiles, warp w takes row tile w % 4 and column group w / 4 (of kQ).
+constexpr int kChunkThreads = 512, kWarps = kChunkThreads / 32, kTPW = 32 / kWarps,
+              kQ = kWarps / 4;
+
 // Row strides of fp32 shared-memory operands.  A warp's fragment read touches rows
 // l/4 and columns l%4 (lane l): a stride of 4 mod 32 puts the 32 reads of a row-major
 // operand in 32 different banks, a stride of 8 mod 32 those of a transposed one.
@@ -129,14 +135,14 @@ constexpr int kLdY = 24;  // 16 x 16 scratch tiles of the solve (read as the B o
 constexpr int kSolveScratch = 8 * 16 * kLdY;
 
 // T = (I + A)^-1 for a strictly lower-triangular 64 x 64 A (row stride lda), written to T
-// (row stride ldt), by 256 threads: the four 16 x 16 diagonal blocks by forward
+// (row stride ldt), by the whole block (at least 4 warps): the four 16 x 16 diagonal blocks by forward
 // substitution, then the blocks below the diagonal by distance d = 1, 2, 3 as
 // T_ij = -T_ii (sum_{k=j}^{i-1} A_ik T_kj), one warp per block pair (tensor tiles).
 // `scratch` holds kSolveScratch floats.  Ends with a __syncthreads().
 __device__ __forceinline__ void solve_unit_lower64(const float *A, int lda, float *T, int ldt,
                                                    float *scratch) {
   const int tid = threadIdx.x, warp = tid >> 5;
-  for (int idx = tid; idx < 64 * 64; idx += 256) {  // blocks above the diagonal are zero
+  for (int idx = tid; idx < 64 * 64; idx += blockDim.x) {  // blocks above the diagonal are zero
     const int i = idx >> 6, j = idx & 63;
     if ((i >> 4) < (j >> 4)) T[i * ldt + j] = 0.f;
   }

@@ -27,7 +27,7 @@ struct PrepSmem {
 };
 
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kChunkThreads)
     k_prep(int32_t group, View k, View v, View g, View beta, View w, View u, View gcum,
            const ChunkInfo *__restrict__ chunks, const int32_t *__restrict__ n_chunks, bool vec) {
   extern __shared__ float sm[];
@@ -40,8 +40,8 @@ __global__ void __launch_bounds__(256)
   float *Ks = sm, *Vs = Ks + 64 * L, *Am = Vs + 64 * L, *Tm = Am + 64 * LA, *TU = Tm + 64 * LA;
   float *G = TU + 64 * LA, *B = G + 64, *BG = B + 64, *scratch = BG + 64;
 
-  tile_bf16<64, D, 256>(Ks, L, bf_row(k, t0, hk), k.st, len, vec);
-  tile_bf16<64, D, 256>(Vs, L, bf_row(v, t0, h), v.st, len, vec);
+  tile_bf16<64, D, kChunkThreads>(Ks, L, bf_row(k, t0, hk), k.st, len, vec);
+  tile_bf16<64, D, kChunkThreads>(Vs, L, bf_row(v, t0, h), v.st, len, vec);
   if (tid < 64) {
     G[tid] = tid < len ? ldf(g.p, (t0 + tid) * g.st + h * g.sh) : 0.f;
     B[tid] = tid < len ? ldbf(beta.p, (t0 + tid) * beta.st + h * beta.sh) : 0.f;
@@ -64,11 +64,11 @@ __global__ void __launch_bounds__(256)
   const int warp = tid >> 5;
   // A_ij = beta_i e^{G_i - G_j} k_i . k_j (j < i): 32 tiles of the key products
   {
-    const int m0 = ((warp * 4) >> 3) * 16, nb = ((warp * 4) & 7) * 8;
-    float accs[4][4] = {};
-    mma_16xN<4>(accs, SMat{Ks, L, 1}, m0, SMat{Ks, 1, L}, nb, 0, D);
+    const int m0 = ((warp * kTPW) >> 3) * 16, nb = ((warp * kTPW) & 7) * 8;
+    float accs[kTPW][4] = {};
+    mma_16xN<kTPW>(accs, SMat{Ks, L, 1}, m0, SMat{Ks, 1, L}, nb, 0, D);
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
+    for (int b = 0; b < kTPW; ++b) {
       const int n0 = nb + 8 * b;
       float(&acc)[4] = accs[b];
 #pragma unroll
@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(256)
   }
   __syncthreads();
   // W = Tm diag(beta e^G) K, U = Tm diag(beta) V: 64 x D outputs each
-  for (int tl = warp; tl < 4 * (D / 8); tl += 8) {
+  for (int tl = warp; tl < 4 * (D / 8); tl += kWarps) {
     const int m0 = (tl & 3) * 16, n0 = (tl >> 2) * 8;
     float wa[4] = {0.f, 0.f, 0.f, 0.f}, ua[4] = {0.f, 0.f, 0.f, 0.f};
     mma_16x8(wa, SMat{Am, LA, 1}, m0, SMat{Ks, L, 1}, n0, 0, 64);
@@ -299,11 +299,11 @@ cudaError_t launch_prep(const StageShapes &s, View k, View v, View g, View beta,
   cudaError_t e;
   if (s.D == 64) {
     if ((e = set_smem(k_prep<64>, PrepSmem<64>::bytes)) != cudaSuccess) return e;
-    k_prep<64><<<grid, 256, PrepSmem<64>::bytes, stream>>>(s.H / s.Hk, k, v, g, beta, w, u,
+    k_prep<64><<<grid, kChunkThreads, PrepSmem<64>::bytes, stream>>>(s.H / s.Hk, k, v, g, beta, w, u,
                                                            gcum, chunks, n_chunks, vec);
   } else {
     if ((e = set_smem(k_prep<128>, PrepSmem<128>::bytes)) != cudaSuccess) return e;
-    k_prep<128><<<grid, 256, PrepSmem<128>::bytes, stream>>>(s.H / s.Hk, k, v, g, beta, w, u,
+    k_prep<128><<<grid, kChunkThreads, PrepSmem<128>::bytes, stream>>>(s.H / s.Hk, k, v, g, beta, w, u,
                                                              gcum, chunks, n_chunks, vec);
   }
   return cudaGetLastError();
