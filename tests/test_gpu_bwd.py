@@ -151,3 +151,47 @@ def test_backward_full_size_packed_sampled_heads():
     for name, i in (("dv", 2), ("dg", 3), ("dbeta", 4)):
         _close(name, got[i][:, hv], ref[i], mask)
     _close("dh0", got[5][:, hv], ref[5])
+
+
+def test_backward_unaligned_views_take_the_scalar_loads():
+    # q, k, v and dout as views whose rows are not 16-byte aligned (an odd element
+    # offset into a larger buffer): the kernels fall back to element loads and must give
+    # the same gradients as the aligned call
+    w = make_workload("unaligned", 61, [130, 0, 70], 1, 2, 64, with_h0=True)
+    do, dht = _upstream(w, 62, True)
+    ref = _run_bwd(w, do, dht)
+    wd = w.to("cuda")
+
+    def shifted(t):
+        buf = torch.empty(t.numel() + 1, dtype=t.dtype, device="cuda")
+        view = buf[1:].view(t.shape)
+        view.copy_(t)
+        return view
+
+    q, k, v, dof = shifted(wd.q), shifted(wd.k), shifted(wd.v), shifted(do.cuda())
+    assert q.data_ptr() % 16 != 0
+    got = api.chunk_bwd(q, k, v, wd.g, wd.beta, dof, scale=w.scale, initial_state=wd.h0,
+                        cu_seqlens=wd.cu_seqlens, dht=dht.cuda(), want_dh0=True)
+    torch.cuda.synchronize()
+    for name, a, b in zip(NAMES, got, ref):
+        assert torch.equal(a, b), name
+
+
+def test_backward_only_empty_segments():
+    # every segment empty: no chunk runs, dh0 is dht, every other gradient is zero
+    w = make_workload("empty", 71, [0, 0, 0], 1, 2, 64, with_h0=True)
+    gen = torch.Generator().manual_seed(72)
+    T = 8  # tokens that no segment covers
+    q = torch.randn(T, 1, 64, generator=gen).to(torch.bfloat16).cuda()
+    v = torch.randn(T, 2, 64, generator=gen).to(torch.bfloat16).cuda()
+    g = -torch.rand(T, 2, generator=gen).cuda()
+    beta = torch.rand(T, 2, generator=gen).to(torch.bfloat16).cuda()
+    do = torch.randn(T, 2, 64, generator=gen).to(torch.bfloat16).cuda()
+    dht = torch.randn(3, 2, 64, 64, generator=gen).cuda()
+    cu = torch.tensor([0, 0, 0, 0], dtype=torch.int32, device="cuda")
+    dq, dk, dv, dg, db, dh0 = api.chunk_bwd(q, q, v, g, beta, do, initial_state=w.h0.cuda(),
+                                            cu_seqlens=cu, dht=dht, want_dh0=True)
+    torch.cuda.synchronize()
+    for t in (dq, dk, dv, dg, db):
+        assert not t.any()
+    assert torch.equal(dh0, dht)

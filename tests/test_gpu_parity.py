@@ -262,3 +262,29 @@ def test_named_workload_full_size(name, path):
     if w.want_ht:
         assert_ht_close(ht[:, heads], ht_ref)
     assert api.device_status() == 0, "a bounded wait ran out"
+
+
+def test_unaligned_inputs_take_the_staged_element_loads():
+    # q, k, v at an odd element offset (rows not 16-byte aligned): the fused path cannot
+    # take them, AUTO runs the staged kernels with element loads, and the result is
+    # bit-identical to the staged path's vector loads on aligned copies (and the fused
+    # path refuses such inputs)
+    w = make_workload("unaligned", 81, [150, 0, 77], 2, 4, 64, with_h0=True)
+    wd = w.to("cuda")
+
+    def shifted(t):
+        buf = torch.empty(t.numel() + 1, dtype=t.dtype, device="cuda")
+        view = buf[1:].view(t.shape)
+        view.copy_(t)
+        return view
+
+    q, k, v = shifted(wd.q), shifted(wd.k), shifted(wd.v)
+    assert q.data_ptr() % 16 != 0
+    kw = dict(scale=w.scale, initial_state=wd.h0, cu_seqlens=wd.cu_seqlens,
+              output_final_state=True)
+    o1, ht1 = api.chunk_fwd(q, k, v, wd.g, wd.beta, path="auto", **kw)
+    o2, ht2 = api.chunk_fwd(wd.q, wd.k, wd.v, wd.g, wd.beta, path="staged", **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(ht1, ht2)
+    with pytest.raises(api.nat.GdrError):
+        api.chunk_fwd(q, k, v, wd.g, wd.beta, path="fused", **kw)
