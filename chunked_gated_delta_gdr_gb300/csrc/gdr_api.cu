@@ -6,6 +6,7 @@
 
 #include "gdr_bwd.cuh"
 #include "gdr_internal.cuh"
+#include "gdr_sched.cuh"
 
 using namespace gdr;
 
@@ -134,6 +135,7 @@ struct IndexWs {
   SegInfo *seg;
   ChunkInfo *chunks;
   int32_t *n_chunks;
+  int32_t *order;  // segments longest first, for the per-segment scans
   size_t bytes;
 };
 
@@ -147,6 +149,8 @@ IndexWs carve_index(void *ws, int64_t T, int32_t n_seq) {
   off += align256(sizeof(SegInfo) * (size_t)(n_seq > 0 ? n_seq : 1));
   r.chunks = reinterpret_cast<ChunkInfo *>(p + off);
   off += align256(sizeof(ChunkInfo) * (size_t)chunk_bound(T, n_seq));
+  r.order = reinterpret_cast<int32_t *>(p + off);
+  off += align256(sizeof(int32_t) * (size_t)(n_seq > 0 ? n_seq : 1));
   r.bytes = off;
   return r;
 }
@@ -267,9 +271,12 @@ int run_fwd(const Problem &P, float scale, const int32_t *cu, int32_t path, void
   e = launch_prep(s, view_of(P.k), view_of(P.v), view_of(P.g), view_of(P.beta), vw, vu, vg,
                   ix.seg, ix.chunks, ix.n_chunks, stream);
   if (e != cudaSuccess) return GDR_ERR_CUDA;
-  e = launch_scan(s, view_of(P.k), vw, vu, vg,
-                  P.has_h0 ? reinterpret_cast<const float *>(P.h0.p) : nullptr, h, vv,
-                  P.has_ht ? reinterpret_cast<float *>(P.ht.p) : nullptr, P.ck, ix.seg, stream);
+  if ((e = launch_seg_order(ix.seg, P.n_seq, ix.order, stream)) != cudaSuccess)
+    return GDR_ERR_CUDA;
+  e = launch_scan_ordered(s, view_of(P.k), vw, vu, vg,
+                          P.has_h0 ? reinterpret_cast<const float *>(P.h0.p) : nullptr, h, vv,
+                          P.has_ht ? reinterpret_cast<float *>(P.ht.p) : nullptr, P.ck, ix.seg,
+                          ix.order, stream);
   if (e != cudaSuccess) return GDR_ERR_CUDA;
   e = launch_out(s, view_of(P.q), view_of(P.k), vv, h, vg, scale, view_of(P.o), ix.seg,
                  ix.chunks, ix.n_chunks, stream);
@@ -478,7 +485,8 @@ int gdr_chunk_bwd(const gdr_tensor_t *q, const gdr_tensor_t *k, const gdr_tensor
   const IndexWs ix = carve_index(workspace, P.T, P.n_seq);
   const int64_t cap = chunk_bound(P.T, P.n_seq);
   if (launch_chunk_index(cu_seqlens, P.n_seq, P.T, ix.seg, ix.chunks, cap, ix.n_chunks,
-                         stream) != cudaSuccess)
+                         stream) != cudaSuccess ||
+      launch_seg_order(ix.seg, P.n_seq, ix.order, stream) != cudaSuccess)
     return GDR_ERR_CUDA;
   BwdArgs a{};
   a.s = StageShapes{P.T, P.n_seq, P.Hk, P.H, P.D, cap};
@@ -498,6 +506,7 @@ int gdr_chunk_bwd(const gdr_tensor_t *q, const gdr_tensor_t *k, const gdr_tensor
   a.dbeta = view_of(Db);
   a.dh0 = dh0 ? reinterpret_cast<float *>(Dh.p) : nullptr;
   a.seg = ix.seg;
+  a.order = ix.order;
   a.chunks = ix.chunks;
   a.n_chunks = ix.n_chunks;
   a.work = reinterpret_cast<char *>(workspace) + ix.bytes;
@@ -613,10 +622,12 @@ int gdr_state_scan(const gdr_tensor_t *k, const gdr_tensor_t *w, const gdr_tenso
   const StageShapes s{T, n_seq, (int32_t)Hk, (int32_t)H, (int32_t)D, cap};
   cudaError_t e = launch_chunk_index(cu_seqlens, n_seq, T, ix.seg, ix.chunks, cap,
                                      ix.n_chunks, stream);
+  if (e == cudaSuccess) e = launch_seg_order(ix.seg, n_seq, ix.order, stream);
   if (e == cudaSuccess)
-    e = launch_scan(s, view_of(K), view_of(Wd), view_of(Ud), view_of(Gc),
-                    h0 ? reinterpret_cast<const float *>(H0.p) : nullptr, Hd.p, view_of(Vn),
-                    ht ? reinterpret_cast<float *>(HT.p) : nullptr, Ckpt{}, ix.seg, stream);
+    e = launch_scan_ordered(s, view_of(K), view_of(Wd), view_of(Ud), view_of(Gc),
+                            h0 ? reinterpret_cast<const float *>(H0.p) : nullptr, Hd.p,
+                            view_of(Vn), ht ? reinterpret_cast<float *>(HT.p) : nullptr, Ckpt{},
+                            ix.seg, ix.order, stream);
   return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 

@@ -37,6 +37,7 @@
 // result is bit-identical from run to run (no atomics).
 #include "gdr_bwd.cuh"
 #include "gdr_mma.cuh"
+#include "gdr_sched.cuh"
 
 namespace gdr {
 namespace {
@@ -117,12 +118,13 @@ template <int D, int kScanCols>
 __global__ void __launch_bounds__(kScanCols * 4)
     k_bwd_scan(int32_t H, int32_t group, View q, View k, View w, View dout, View gcum,
                float scale, const float *dht, View dvp, float *dh, float *dh0,
-               const SegInfo *__restrict__ seg, bool vec) {
+               const SegInfo *__restrict__ seg, const int32_t *__restrict__ order, bool vec) {
   extern __shared__ float sm[];
   using Sm = BwdScanSmem<D, kScanCols>;
   constexpr int LK = Sm::kLdK, LQ = Sm::kLdQ, LC = Sm::kLdC;
   constexpr int NT = kScanCols * 4, NW = kScanCols / 8, CT = kScanCols / 8;  // threads, warps, column tiles
-  const int n = blockIdx.x, h = blockIdx.y, jb = blockIdx.z * kScanCols, tid = threadIdx.x;
+  // grid (head, column block, segment rank): the longest segments are dispatched first
+  const int n = order[blockIdx.z], h = blockIdx.x, jb = blockIdx.y * kScanCols, tid = threadIdx.x;
   const int hk = h / group;
   const SegInfo si = seg[n];
   float *dS = sm, *Ks = dS + D * LC, *Ws = Ks + 64 * LK, *Qs = Ws + 64 * LQ, *Dos = Qs + 64 * LQ;
@@ -711,8 +713,8 @@ cudaError_t launch_bwd_d(const BwdArgs &a, const BwdWs &w, cudaStream_t stream) 
   if ((e = launch_prep(s, a.k, a.v, a.g, a.beta, vw, vu, vg, a.seg, a.chunks, a.n_chunks,
                        stream)) != cudaSuccess)
     return e;
-  if ((e = launch_scan(s, a.k, vw, vu, vg, a.h0, w.h, vn, nullptr, Ckpt{nullptr, nullptr, 0},
-                       a.seg, stream)) != cudaSuccess)
+  if ((e = launch_scan_ordered(s, a.k, vw, vu, vg, a.h0, w.h, vn, nullptr,
+                               Ckpt{nullptr, nullptr, 0}, a.seg, a.order, stream)) != cudaSuccess)
     return e;
   const dim3 gc((unsigned)s.chunk_cap, (unsigned)s.H);
   if ((e = set_smem(k_bwd_dv_intra<D>, DvIntraSmem<D>::bytes)) != cudaSuccess) return e;
@@ -722,8 +724,9 @@ cudaError_t launch_bwd_d(const BwdArgs &a, const BwdWs &w, cudaStream_t stream) 
   auto scan = [&](auto kern, int cols, size_t bytes) -> cudaError_t {
     cudaError_t r = set_smem(kern, bytes);
     if (r != cudaSuccess) return r;
-    kern<<<dim3((unsigned)s.n_seq, (unsigned)s.H, (unsigned)(D / cols)), cols * 4, bytes, stream>>>(
-        s.H, group, a.q, a.k, vw, a.dout, vg, a.scale, a.dht, vdvp, w.dh, a.dh0, a.seg, vec);
+    kern<<<dim3((unsigned)s.H, (unsigned)(D / cols), (unsigned)s.n_seq), cols * 4, bytes, stream>>>(
+        s.H, group, a.q, a.k, vw, a.dout, vg, a.scale, a.dht, vdvp, w.dh, a.dh0, a.seg, a.order,
+        vec);
     return cudaGetLastError();
   };
   e = scan_cols(s.n_seq, s.H, D) == 64 ? scan(k_bwd_scan<D, 64>, 64, BwdScanSmem<D, 64>::bytes)

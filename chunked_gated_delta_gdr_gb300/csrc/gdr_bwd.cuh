@@ -17,6 +17,7 @@ struct BwdArgs {
   View dq, dk, dv, dg, dbeta;  // outputs (fp32)
   float *dh0;                  // [n_seq, H, D, D] or null
   const SegInfo *seg;
+  const int32_t *order;        // segments longest first (launch_seg_order)
   const ChunkInfo *chunks;
   const int32_t *n_chunks;
   void *work;                  // gdr_bwd_work_bytes bytes, 256-byte aligned

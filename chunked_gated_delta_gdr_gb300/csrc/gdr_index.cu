@@ -10,6 +10,7 @@
 // non-decreasing by a running maximum; segment n is [c[n], c[n+1]).
 // Length-0 segments ("Findings ...", section 2) get zero chunks.
 #include "gdr_internal.cuh"
+#include "gdr_sched.cuh"
 
 namespace gdr {
 namespace {
@@ -130,6 +131,26 @@ __global__ void __launch_bounds__(kScanThreads)
   if (threadIdx.x == 0) off[n_seq] = carry;
 }
 
+// Segments by chunk count, longest first: counting sort over kScanThreads buckets
+// (counts beyond the last bucket share it); positions within a bucket are arbitrary.
+__global__ void __launch_bounds__(kScanThreads)
+    k_seg_order(const SegInfo *__restrict__ seg, int32_t n_seq, int32_t *order) {
+  __shared__ int warp_buf[32];
+  __shared__ int pos[kScanThreads];
+  const int b0 = threadIdx.x;
+  pos[b0] = 0;
+  __syncthreads();
+  auto bucket = [](int nc) { return kScanThreads - 1 - min(nc, kScanThreads - 1); };
+  for (int n = threadIdx.x; n < n_seq; n += kScanThreads) atomicAdd(&pos[bucket(seg[n].n_chunks)], 1);
+  __syncthreads();
+  const int x = pos[b0];
+  const int incl = block_inclusive_scan<false>(x, warp_buf);
+  pos[b0] = incl - x;
+  __syncthreads();
+  for (int n = threadIdx.x; n < n_seq; n += kScanThreads)
+    order[atomicAdd(&pos[bucket(seg[n].n_chunks)], 1)] = n;
+}
+
 __global__ void k_check_cu(const int32_t *__restrict__ cu, int32_t n_seq, int64_t T,
                            int32_t *out2) {
   // out2[0]: count of bad offsets, out2[1]: first bad index (or -1); single block
@@ -164,6 +185,13 @@ cudaError_t launch_chunk_index(const int32_t *cu, int32_t n_seq, int64_t T, SegI
   int64_t blocks = ceil_div64(chunk_cap, threads);
   if (blocks > 4096) blocks = 4096;
   k_chunk_table<<<(unsigned)blocks, threads, 0, stream>>>(seg, n_seq, n_chunks, chunks, chunk_cap);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_seg_order(const SegInfo *seg, int32_t n_seq, int32_t *order,
+                             cudaStream_t stream) {
+  if (n_seq <= 0) return cudaSuccess;
+  k_seg_order<<<1, kScanThreads, 0, stream>>>(seg, n_seq, order);
   return cudaGetLastError();
 }
 

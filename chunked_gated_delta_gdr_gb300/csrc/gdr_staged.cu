@@ -14,6 +14,7 @@
 // integrating FlashQLA's Blackwell GDN kernels into a JAX trainer", section 1).
 #include "gdr_internal.cuh"
 #include "gdr_mma.cuh"
+#include "gdr_sched.cuh"
 
 namespace gdr {
 namespace {
@@ -119,12 +120,14 @@ template <int D, int kScanCols>
 __global__ void __launch_bounds__(kScanCols * 4)
     k_scan(int32_t H, int32_t group, View k, View w, View u, View gcum, const float *h0,
            __nv_bfloat16 *hbuf, View v_new, float *ht, Ckpt ck,
-           const SegInfo *__restrict__ seg, bool vec) {
+           const SegInfo *__restrict__ seg, const int32_t *__restrict__ order, bool vec) {
   extern __shared__ float sm[];
   using Sm = ScanSmem<D, kScanCols>;
   constexpr int LW = Sm::kLdW, LK = Sm::kLdK, LC = Sm::kLdC;
   constexpr int NT = kScanCols * 4, NW = kScanCols / 8, CT = kScanCols / 8;  // threads, warps, column tiles
-  const int n = blockIdx.x, h = blockIdx.y, jb = blockIdx.z * kScanCols, tid = threadIdx.x;
+  // grid (head, column block, segment rank): the longest segments are dispatched first
+  const int n = order ? order[blockIdx.z] : (int)blockIdx.z, h = blockIdx.x;
+  const int jb = blockIdx.y * kScanCols, tid = threadIdx.x;
   const int hk = h / group;
   const SegInfo si = seg[n];
   float *S = sm, *Ws = S + D * LC, *Ks = Ws + 64 * LW, *Us = Ks + 64 * LK, *Vn = Us + 64 * LC;
@@ -312,14 +315,20 @@ cudaError_t launch_prep(const StageShapes &s, View k, View v, View g, View beta,
 cudaError_t launch_scan(const StageShapes &s, View k, View w, View u, View gcum,
                         const float *h0, void *h, View v_new, float *ht, Ckpt ck,
                         const SegInfo *seg, cudaStream_t stream) {
+  return launch_scan_ordered(s, k, w, u, gcum, h0, h, v_new, ht, ck, seg, nullptr, stream);
+}
+
+cudaError_t launch_scan_ordered(const StageShapes &s, View k, View w, View u, View gcum,
+                                const float *h0, void *h, View v_new, float *ht, Ckpt ck,
+                                const SegInfo *seg, const int32_t *order, cudaStream_t stream) {
   if (s.n_seq <= 0 || s.H <= 0) return cudaSuccess;
   auto *hb = reinterpret_cast<__nv_bfloat16 *>(h);
   const bool vec = vec_ok(k) && vec_ok(w) && vec_ok(u);
   auto scan = [&](auto kern, int cols, size_t bytes) -> cudaError_t {
     cudaError_t r = set_smem(kern, bytes);
     if (r != cudaSuccess) return r;
-    kern<<<dim3((unsigned)s.n_seq, (unsigned)s.H, (unsigned)(s.D / cols)), cols * 4, bytes,
-           stream>>>(s.H, s.H / s.Hk, k, w, u, gcum, h0, hb, v_new, ht, ck, seg, vec);
+    kern<<<dim3((unsigned)s.H, (unsigned)(s.D / cols), (unsigned)s.n_seq), cols * 4, bytes,
+           stream>>>(s.H, s.H / s.Hk, k, w, u, gcum, h0, hb, v_new, ht, ck, seg, order, vec);
     return cudaGetLastError();
   };
   const bool wide = scan_cols(s.n_seq, s.H, s.D) == 64;
