@@ -434,7 +434,8 @@ template <int D>
 struct WySmem {
   static constexpr int kLd = ld_rows(D), kLdK = ld_rows(64), kLdT = ld_cols(64);
   static constexpr size_t bytes =
-      sizeof(float) * (4 * 64 * kLd + 64 * kLdK + 3 * 64 * kLdT + (5 + 4 * kQ) * 64);
+      sizeof(float) * (4 * 64 * kLd + 64 * kLdK + 3 * 64 * kLdT + (5 + 4 * kQ) * 64 +
+                       kSolveScratch);
 };
 
 template <int D>
@@ -454,6 +455,7 @@ __global__ void __launch_bounds__(kChunkThreads)
   float *KK = dWs + 64 * L, *Tm = KK + 64 * LK, *dT = Tm + 64 * LT, *X = dT + 64 * LT;
   float *G = X + 64 * LT, *B = G + 64, *BG = B + 64, *EGv = BG + 64, *dGt = EGv + 64;
   float *baP = dGt + 64, *bbP = baP + kQ * 64;  // [kQ][64] partial row sums
+  float *scratch = bbP + kQ * 64;
   const float *dvt = reinterpret_cast<const float *>(dvp.p), *dwt = reinterpret_cast<const float *>(dw.p);
   tile_bf16<64, D, kChunkThreads>(Ks, L, bf_row(k, t0, hk), k.st, len, vec);
   tile_bf16<64, D, kChunkThreads>(Vs, L, bf_row(v, t0, h), v.st, len, vec);
@@ -501,18 +503,18 @@ __global__ void __launch_bounds__(kChunkThreads)
     }
   }
   __syncthreads();
-  solve_unit_lower64(X, LT, Tm, LT, dT);  // T = (I + A)^-1; dT's space as scratch until it is formed
-  // dT_ij = beta_j (dU_i . v_j) + beta_j e^{G_j} (dW_i . k_j), i > j (the only part dA needs)
-  {
-    const int m0 = ((warp * kTPW) >> 3) * 16, nb = ((warp * kTPW) & 7) * 8;
-    float dus[kTPW][4] = {}, dwks[kTPW][4] = {};
-    mma_16xN<kTPW>(dus, SMat{dVs, L, 1}, m0, SMat{Vs, 1, L}, nb, 0, D);
-    mma_16xN<kTPW>(dwks, SMat{dWs, L, 1}, m0, SMat{Ks, 1, L}, nb, 0, D);
-#pragma unroll
-    for (int b = 0; b < kTPW; ++b) {
-      const int n0 = nb + 8 * b;
-      float(&du)[4] = dus[b];
-      float(&dwk)[4] = dwks[b];
+  constexpr int kSolveWarps = 4;
+  if (warp < kSolveWarps) {
+    // T = (I + A)^-1 on warps 0-3 (named barrier 1) ...
+    solve_unit_lower64(X, LT, Tm, LT, scratch, kSolveWarps * 32, 1);
+  } else {
+    // ... while the others form dT_ij = beta_j (dU_i . v_j) + beta_j e^{G_j} (dW_i . k_j),
+    // i > j (the only part dA needs), which does not need T
+    for (int tl = warp - kSolveWarps; tl < 32; tl += kWarps - kSolveWarps) {
+      const int m0 = (tl >> 3) * 16, n0 = (tl & 7) * 8;
+      float du[4] = {0.f, 0.f, 0.f, 0.f}, dwk[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_16x8(du, SMat{dVs, L, 1}, m0, SMat{Vs, 1, L}, n0, 0, D);
+      mma_16x8(dwk, SMat{dWs, L, 1}, m0, SMat{Ks, 1, L}, n0, 0, D);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = acc_row(m0, e), j = acc_col(n0, e);
@@ -595,15 +597,25 @@ __global__ void __launch_bounds__(kChunkThreads)
     bbP[cg * 64 + r0 + 8] = bb[1];
   }
   __syncthreads();
-  if (tid < 64) {
-    const int r = tid;
+  {
+    // row r = tid / 8; its 8 threads (neighbouring lanes) take every 8th index, then
+    // three shuffles add the parts in a fixed order
+    const int r = tid >> 3, part = tid & 7;
     float dbc = 0.f, rowq = 0.f, colq = 0.f;
     if (r < len) {
-      for (int x = 0; x < r; ++x) {
+      for (int x = part; x < r; x += 8) {
         dbc += dT[r * LT + x] * expf(G[r] - G[x]) * KK[r * LK + x];
         rowq += X[r * LT + x] * KK[r * LK + x];
       }
-      for (int a = r + 1; a < len; ++a) colq += X[a * LT + r] * KK[a * LK + r];
+      for (int a = r + 1 + part; a < len; a += 8) colq += X[a * LT + r] * KK[a * LK + r];
+    }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      dbc += __shfl_xor_sync(0xffffffffu, dbc, o);
+      rowq += __shfl_xor_sync(0xffffffffu, rowq, o);
+      colq += __shfl_xor_sync(0xffffffffu, colq, o);
+    }
+    if (r < len && part == 0) {
       float dba = 0.f, dbb = 0.f;
       for (int q = 0; q < kQ; ++q) {
         dba += baP[q * 64 + r];

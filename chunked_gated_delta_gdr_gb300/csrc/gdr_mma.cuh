@@ -134,15 +134,22 @@ __host__ __device__ constexpr int ld_cols(int cols) { return cols + 8; }   // re
 constexpr int kLdY = 24;  // 16 x 16 scratch tiles of the solve (read as the B operand)
 constexpr int kSolveScratch = 8 * 16 * kLdY;
 
+// Synchronise the first `nthreads` threads of the block on named barrier `id` (id 0 with
+// the whole block is __syncthreads).
+__device__ __forceinline__ void bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // T = (I + A)^-1 for a strictly lower-triangular 64 x 64 A (row stride lda), written to T
-// (row stride ldt), by the whole block (at least 4 warps): the four 16 x 16 diagonal blocks by forward
-// substitution, then the blocks below the diagonal by distance d = 1, 2, 3 as
+// (row stride ldt), by threads 0 .. nthreads-1 of the block (at least 4 warps, whole
+// warps) synchronised on named barrier `bar`: the four 16 x 16 diagonal blocks by
+// forward substitution, then the blocks below the diagonal by distance d = 1, 2, 3 as
 // T_ij = -T_ii (sum_{k=j}^{i-1} A_ik T_kj), one warp per block pair (tensor tiles).
-// `scratch` holds kSolveScratch floats.  Ends with a __syncthreads().
+// `scratch` holds kSolveScratch floats.  Ends with that barrier.
 __device__ __forceinline__ void solve_unit_lower64(const float *A, int lda, float *T, int ldt,
-                                                   float *scratch) {
+                                                   float *scratch, int nthreads, int bar) {
   const int tid = threadIdx.x, warp = tid >> 5;
-  for (int idx = tid; idx < 64 * 64; idx += blockDim.x) {  // blocks above the diagonal are zero
+  for (int idx = tid; idx < 64 * 64; idx += nthreads) {  // blocks above the diagonal are zero
     const int i = idx >> 6, j = idx & 63;
     if ((i >> 4) < (j >> 4)) T[i * ldt + j] = 0.f;
   }
@@ -154,7 +161,7 @@ __device__ __forceinline__ void solve_unit_lower64(const float *A, int lda, floa
       T[(o + i) * ldt + o + c] = x;
     }
   }
-  __syncthreads();
+  bar_sync(bar, nthreads);
   for (int dist = 1; dist < 4; ++dist) {
     if (warp < 4 - dist) {
       const int j = warp, i = warp + dist;
@@ -181,7 +188,7 @@ __device__ __forceinline__ void solve_unit_lower64(const float *A, int lda, floa
       }
       __syncwarp();
     }
-    __syncthreads();
+    bar_sync(bar, nthreads);
   }
 }
 

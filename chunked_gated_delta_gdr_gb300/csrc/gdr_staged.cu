@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kChunkThreads)
     }
   }
   __syncthreads();
-  solve_unit_lower64(Am, LA, Tm, LA, scratch);  // Tm = (I + A)^-1
+  solve_unit_lower64(Am, LA, Tm, LA, scratch, blockDim.x, 0);  // Tm = (I + A)^-1
   // Tm diag(beta e^G) into Am's place, Tm diag(beta) into TU
   for (int idx = tid; idx < 64 * 64; idx += blockDim.x) {
     const int i = idx >> 6, j = idx & 63;
