@@ -123,8 +123,11 @@ __global__ void __launch_bounds__(kScanCols * 4)
   using Sm = BwdScanSmem<D, kScanCols>;
   constexpr int LK = Sm::kLdK, LQ = Sm::kLdQ, LC = Sm::kLdC;
   constexpr int NT = kScanCols * 4, NW = kScanCols / 8, CT = kScanCols / 8;  // threads, warps, column tiles
-  // grid (head, column block, segment rank): the longest segments are dispatched first
-  const int n = order[blockIdx.z], h = blockIdx.x, jb = blockIdx.y * kScanCols, tid = threadIdx.x;
+  // one flat grid, head fastest, then column block, then segment rank: the longest
+  // segments are dispatched first (a flat x extent allows any segment count)
+  const int64_t bid = blockIdx.x, Z = D / kScanCols;
+  const int h = (int)(bid % H), n = order[bid / H / Z];
+  const int jb = (int)((bid / H) % Z) * kScanCols, tid = threadIdx.x;
   const int hk = h / group;
   const SegInfo si = seg[n];
   float *dS = sm, *Ks = dS + D * LC, *Ws = Ks + 64 * LK, *Qs = Ws + 64 * LQ, *Dos = Qs + 64 * LQ;
@@ -736,9 +739,10 @@ cudaError_t launch_bwd_d(const BwdArgs &a, const BwdWs &w, cudaStream_t stream) 
   auto scan = [&](auto kern, int cols, size_t bytes) -> cudaError_t {
     cudaError_t r = set_smem(kern, bytes);
     if (r != cudaSuccess) return r;
-    kern<<<dim3((unsigned)s.H, (unsigned)(D / cols), (unsigned)s.n_seq), cols * 4, bytes, stream>>>(
-        s.H, group, a.q, a.k, vw, a.dout, vg, a.scale, a.dht, vdvp, w.dh, a.dh0, a.seg, a.order,
-        vec);
+    const int64_t blocks = (int64_t)s.H * (D / cols) * s.n_seq;
+    kern<<<(unsigned)blocks, cols * 4, bytes, stream>>>(s.H, group, a.q, a.k, vw, a.dout, vg,
+                                                       a.scale, a.dht, vdvp, w.dh, a.dh0, a.seg,
+                                                       a.order, vec);
     return cudaGetLastError();
   };
   e = scan_cols(s.n_seq, s.H, D) == 64 ? scan(k_bwd_scan<D, 64>, 64, BwdScanSmem<D, 64>::bytes)

@@ -125,9 +125,12 @@ __global__ void __launch_bounds__(kScanCols * 4)
   using Sm = ScanSmem<D, kScanCols>;
   constexpr int LW = Sm::kLdW, LK = Sm::kLdK, LC = Sm::kLdC;
   constexpr int NT = kScanCols * 4, NW = kScanCols / 8, CT = kScanCols / 8;  // threads, warps, column tiles
-  // grid (head, column block, segment rank): the longest segments are dispatched first
-  const int n = order ? order[blockIdx.z] : (int)blockIdx.z, h = blockIdx.x;
-  const int jb = blockIdx.y * kScanCols, tid = threadIdx.x;
+  // one flat grid, head fastest, then column block, then segment rank: the longest
+  // segments are dispatched first (a flat x extent allows any segment count)
+  const int64_t bid = blockIdx.x, Z = D / kScanCols;
+  const int h = (int)(bid % H), rank = (int)(bid / H / Z);
+  const int n = order ? order[rank] : rank;
+  const int jb = (int)((bid / H) % Z) * kScanCols, tid = threadIdx.x;
   const int hk = h / group;
   const SegInfo si = seg[n];
   float *S = sm, *Ws = S + D * LC, *Ks = Ws + 64 * LW, *Us = Ks + 64 * LK, *Vn = Us + 64 * LC;
@@ -327,8 +330,9 @@ cudaError_t launch_scan_ordered(const StageShapes &s, View k, View w, View u, Vi
   auto scan = [&](auto kern, int cols, size_t bytes) -> cudaError_t {
     cudaError_t r = set_smem(kern, bytes);
     if (r != cudaSuccess) return r;
-    kern<<<dim3((unsigned)s.H, (unsigned)(s.D / cols), (unsigned)s.n_seq), cols * 4, bytes,
-           stream>>>(s.H, s.H / s.Hk, k, w, u, gcum, h0, hb, v_new, ht, ck, seg, order, vec);
+    const int64_t blocks = (int64_t)s.H * (s.D / cols) * s.n_seq;
+    kern<<<(unsigned)blocks, cols * 4, bytes, stream>>>(s.H, s.H / s.Hk, k, w, u, gcum, h0, hb,
+                                                       v_new, ht, ck, seg, order, vec);
     return cudaGetLastError();
   };
   const bool wide = scan_cols(s.n_seq, s.H, s.D) == 64;

@@ -195,3 +195,28 @@ def test_backward_only_empty_segments():
     for t in (dq, dk, dv, dg, db):
         assert not t.any()
     assert torch.equal(dh0, dht)
+
+
+def test_more_segments_than_a_grid_dimension_holds():
+    # 70000 segments (a grid's y and z extents stop at 65535): a few real ones among
+    # empty ones; both forward paths and the backward against the oracle
+    lens = [0] * 70000
+    for i, L in ((3, 90), (40000, 64), (69998, 7)):
+        lens[i] = L
+    w = make_workload("many_segments", 91, lens, 1, 2, 64, with_h0=False)
+    o_ref, ht_ref = oracle.recurrent(w.q, w.k, w.v, w.g, w.beta, w.scale, None, w.cu_seqlens)
+    wd = w.to("cuda")
+    mask = covered_tokens(w.cu_seqlens, w.T)
+    for path in ("staged", "fused"):
+        o, ht = api.chunk_fwd(wd.q, wd.k, wd.v, wd.g, wd.beta, scale=w.scale,
+                              cu_seqlens=wd.cu_seqlens, output_final_state=True, path=path)
+        torch.cuda.synchronize()
+        err = float(np.abs(o.float().cpu().numpy()[mask] - o_ref[mask]).max())
+        assert err <= 4e-3, (path, err)
+        rel = float(np.abs(ht.cpu().numpy() - ht_ref).max() / np.abs(ht_ref).max())
+        assert rel <= 1e-2, (path, rel)
+    do, dht = _upstream(w, 92, False)
+    got = _run_bwd(w, do, dht)
+    ref = oracle.recurrent_bwd(w.q, w.k, w.v, w.g, w.beta, w.scale, None, w.cu_seqlens, do, None)
+    for name, a, b in zip(NAMES[:5], got[:5], ref[:5]):
+        _close(name, a, b, mask)
