@@ -89,6 +89,10 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor
     """
     host = q.device.type == "cpu"
     if host:
+        piped = _chunk_fwd_host_pipelined(q, k, v, g, beta, scale, initial_state, cu_seqlens,
+                                          output_final_state, path, out, final_state)
+        if piped is not None:
+            return piped
         dev = torch.device("cuda", torch.cuda.current_device())
         mv = lambda t: None if t is None else t.to(dev, non_blocking=True)
         q, k, v, g, beta, initial_state = map(mv, (q, k, v, g, beta, initial_state))
@@ -125,6 +129,120 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor
         torch.cuda.current_stream().synchronize()
         return o_h, ht_h
     return o, ht
+
+
+def _segment_bounds(cu, T: int):
+    """Segment bounds after the library's reading of cu_seqlens (clamped to [0, T],
+    made non-decreasing by a running maximum)."""
+    b, prev = [], 0
+    for i, c in enumerate(int(x) for x in cu):
+        c = min(max(c, 0), T)
+        if i > 0 and c < prev:
+            c = prev
+        b.append(c)
+        prev = c
+    return b
+
+
+def _segment_groups(bounds, parts: int):
+    """Cut the segments into at most `parts` runs of consecutive segments with about
+    equal token counts: [(first segment, end segment), ...], none without tokens."""
+    n, total = len(bounds) - 1, bounds[-1] - bounds[0]
+    groups, n0 = [], 0
+    for gi in range(parts):
+        target = bounds[0] + total * (gi + 1) // parts
+        n1 = n0
+        while n1 < n and (bounds[n1] < target or n1 == n0):
+            n1 += 1
+        if gi == parts - 1:
+            n1 = n
+        if bounds[n1] > bounds[n0]:
+            groups.append((n0, n1))
+        elif groups and n1 > n0:
+            groups[-1] = (groups[-1][0], n1)  # trailing empty segments join the last run
+        n0 = n1
+        if n0 >= n:
+            break
+    if groups and groups[-1][1] < n:
+        groups[-1] = (groups[-1][0], n)
+    return groups
+
+
+_PIPE_MIN_TOKENS = 16384  # below this one copy-compute-copy sequence is as fast
+_PIPE_PARTS = 4
+
+
+def _chunk_fwd_host_pipelined(q, k, v, g, beta, scale, initial_state, cu_seqlens,
+                              output_final_state, path, out, final_state, parts=_PIPE_PARTS,
+                              min_tokens=_PIPE_MIN_TOKENS):
+    """Host tensors: cut the packed tokens at segment boundaries into a few runs and give
+    each run its own stream (copy in, forward, copy out), so that uploads use parallel
+    copy engines and downloads overlap later uploads.  Segments are independent and each
+    run computes its segments exactly as one call would (whole, never split into
+    pieces), so the results are bit-identical to a single call.  Returns None when the
+    call is too small, has a single run, or would use the sequence split."""
+    T, Hk, dk = q.shape
+    H, dv = v.shape[1], v.shape[2]
+    if cu_seqlens is None or path not in ("auto", "fused", "fused_whole") or parts < 2:
+        return None
+    if T < min_tokens:
+        return None
+    n_seq = cu_seqlens.numel() - 1
+    if path != "fused_whole" and split_pieces(T, n_seq, H) > 1:
+        return None
+    if not all(t.is_pinned() for t in (q, k, v, g, beta)):
+        return None
+    bounds = _segment_bounds(cu_seqlens.tolist(), T)
+    groups = _segment_groups(bounds, parts)
+    if len(groups) < 2:
+        return None
+    dev = torch.device("cuda", torch.cuda.current_device())
+    main = torch.cuda.current_stream(dev)
+    if scale is None:
+        scale = dk ** -0.5
+    o_h = out if out is not None else torch.empty(T, H, dv, dtype=torch.bfloat16,
+                                                  pin_memory=True)
+    ht_h = None
+    if output_final_state:
+        ht_h = final_state if final_state is not None else torch.empty(
+            n_seq, H, dk, dv, dtype=torch.float32, pin_memory=True)
+    bufs = {name: torch.empty(t.shape, dtype=t.dtype, device=dev)
+            for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta))}
+    o_d = torch.empty(T, H, dv, dtype=torch.bfloat16, device=dev)
+    h0_d = (torch.empty(initial_state.shape, dtype=initial_state.dtype, device=dev)
+            if initial_state is not None else None)
+    ht_d = torch.empty(n_seq, H, dk, dv, dtype=torch.float32, device=dev) if ht_h is not None else None
+    # fused path (the device copies are aligned) with every (segment, head) whole
+    gpath = "fused_whole" if path in ("auto", "fused", "fused_whole") else path
+    work = [(_workspace(workspace_bytes(bounds[n1] - bounds[n0], n1 - n0, H, dk, dv, gpath), dev))
+            for n0, n1 in groups]
+    cus = [torch.tensor([b - bounds[n0] for b in bounds[n0:n1 + 1]], dtype=torch.int32)
+           .pin_memory() for n0, n1 in groups]
+    ready = torch.cuda.Event()
+    ready.record(main)
+    streams = [torch.cuda.Stream(dev) for _ in groups]
+    for (n0, n1), st, ws, cu_h in zip(groups, streams, work, cus):
+        st.wait_event(ready)
+        t0, t1 = bounds[n0], bounds[n1]
+        with torch.cuda.stream(st):
+            for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
+                bufs[name][t0:t1].copy_(t[t0:t1], non_blocking=True)
+            cu_d = cu_h.to(dev, non_blocking=True)
+            h0g = None
+            if h0_d is not None:
+                h0_d[n0:n1].copy_(initial_state[n0:n1], non_blocking=True)
+                h0g = h0_d[n0:n1]
+            chunk_fwd(bufs["q"][t0:t1], bufs["k"][t0:t1], bufs["v"][t0:t1], bufs["g"][t0:t1],
+                      bufs["beta"][t0:t1], scale=scale, initial_state=h0g, cu_seqlens=cu_d,
+                      output_final_state=ht_d is not None, path=gpath, workspace=ws,
+                      out=o_d[t0:t1], final_state=None if ht_d is None else ht_d[n0:n1],
+                      stream=st)
+            o_h[t0:t1].copy_(o_d[t0:t1], non_blocking=True)
+            if ht_d is not None:
+                ht_h[n0:n1].copy_(ht_d[n0:n1], non_blocking=True)
+    for st in streams:
+        st.synchronize()
+    return o_h, ht_h
 
 
 def bwd_workspace_bytes(T: int, n_seq: int, Hk: int, H: int, dk: int, dv: int) -> int:

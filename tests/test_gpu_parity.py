@@ -288,3 +288,20 @@ def test_unaligned_inputs_take_the_staged_element_loads():
     assert torch.equal(o1, o2) and torch.equal(ht1, ht2)
     with pytest.raises(api.nat.GdrError):
         api.chunk_fwd(q, k, v, wd.g, wd.beta, path="fused", **kw)
+
+
+@pytest.mark.parametrize("parts", [2, 3, 4])
+def test_pipelined_host_forward_matches_device(parts):
+    # host tensors cut into runs of whole segments, one stream each (copy in, forward,
+    # copy out): bit-identical to one device call, ht included
+    lens = [700, 0, 1300, 64, 1, 900, 0, 2048, 333, 1000, 0]
+    w = make_workload("pipelined", 77, lens, 4, 8, 64, with_h0=True)
+    assert api.split_pieces(w.T, w.n_seq, w.H) == 1
+    o_d, ht_d = run_gpu(w)
+    pin = lambda t: None if t is None else t.pin_memory()
+    o_h, ht_h = api._chunk_fwd_host_pipelined(pin(w.q), pin(w.k), pin(w.v), pin(w.g),
+                                              pin(w.beta), w.scale, pin(w.h0), w.cu_seqlens,
+                                              True, "auto", None, None, parts=parts,
+                                              min_tokens=0)
+    mask = torch.from_numpy(covered_tokens(w.cu_seqlens, w.T))
+    assert torch.equal(o_h[mask], o_d.cpu()[mask]) and torch.equal(ht_h, ht_d.cpu())
