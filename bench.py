@@ -512,9 +512,15 @@ def bench_ours_bwd(args):
         hh0 = None if w.h0 is None else w.h0.pin_memory()
         hdht = None if dht_h is None else dht_h.pin_memory()
 
+        f32 = dict(dtype=torch.float32, pin_memory=True)
+        outs_h = (torch.empty(w.T, w.Hk, w.dk, **f32), torch.empty(w.T, w.Hk, w.dk, **f32),
+                  torch.empty(w.T, w.H, w.dv, **f32), torch.empty(w.T, w.H, **f32),
+                  torch.empty(w.T, w.H, **f32),
+                  torch.empty(w.n_seq, w.H, w.dk, w.dv, **f32) if want_dh0 else None)
+
         def step_host():
             return api.chunk_bwd(*hs, scale=w.scale, initial_state=hh0, cu_seqlens=w.cu_seqlens,
-                                 dht=hdht, want_dh0=want_dh0, workspace=work)
+                                 dht=hdht, want_dh0=want_dh0, workspace=work, out=outs_h)
 
         step_host()
         torch.cuda.synchronize()

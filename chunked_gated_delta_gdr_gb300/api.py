@@ -254,27 +254,34 @@ def chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor
               initial_state: Optional[torch.Tensor] = None,
               cu_seqlens: Optional[torch.Tensor] = None, dht: Optional[torch.Tensor] = None,
               want_dh0: bool = True, workspace: Optional[torch.Tensor] = None,
-              stream: Optional[torch.cuda.Stream] = None):
+              stream: Optional[torch.cuda.Stream] = None, out: Optional[tuple] = None):
     """Backward of ``chunk_fwd`` (libgdr ``gdr_chunk_bwd``): gradients of the loss with
     respect to q, k, v, g, beta and the initial state, given dout = dL/do [T, H, dv] bf16
     and dht = dL/dht [N, H, dk, dv] f32 (None: zero).
 
     Returns (dq [T, Hk, dk], dk [T, Hk, dk], dv [T, H, dv], dg [T, H], dbeta [T, H],
-    dh0 [N, H, dk, dv] or None), all fp32 on the inputs' device.  Host (CPU) inputs are
-    copied to the current CUDA device, and the gradients back into pinned host tensors.
+    dh0 [N, H, dk, dv] or None), all fp32 on the inputs' device; ``out`` may give these six
+    tensors (compact, fp32, on that device; dh0 may be None) to be written instead.  Host
+    (CPU) inputs are copied to the current CUDA device, and the gradients back into pinned
+    host tensors (``out`` then names host tensors).
     """
     if q.device.type == "cpu":
+        piped = _chunk_bwd_host_pipelined(q, k, v, g, beta, dout, scale, initial_state,
+                                          cu_seqlens, dht, want_dh0, out)
+        if piped is not None:
+            return piped
         dev = torch.device("cuda", torch.cuda.current_device())
         mv = lambda t: None if t is None else t.to(dev, non_blocking=True)
         res = chunk_bwd(*map(mv, (q, k, v, g, beta, dout)), scale=scale,
                         initial_state=mv(initial_state), cu_seqlens=mv(cu_seqlens), dht=mv(dht),
                         want_dh0=want_dh0, workspace=workspace, stream=stream)
         outs = []
-        for t in res:
+        for i, t in enumerate(res):
             if t is None:
                 outs.append(None)
                 continue
-            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            h = out[i] if out is not None else torch.empty(t.shape, dtype=t.dtype,
+                                                           pin_memory=True)
             h.copy_(t, non_blocking=True)
             outs.append(h)
         torch.cuda.current_stream().synchronize()
@@ -288,9 +295,15 @@ def chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor
     if scale is None:
         scale = dk_ ** -0.5
     f32 = dict(dtype=torch.float32, device=dev)
-    dq, dkk = torch.empty(T, Hk, dk_, **f32), torch.empty(T, Hk, dk_, **f32)
-    dvv, dg, db = torch.empty(T, H, dv_, **f32), torch.empty(T, H, **f32), torch.empty(T, H, **f32)
-    dh0 = torch.empty(n_seq, H, dk_, dv_, **f32) if want_dh0 else None
+    if out is not None:
+        dq, dkk, dvv, dg, db, dh0 = out
+        if not want_dh0:
+            dh0 = None
+    else:
+        dq, dkk = torch.empty(T, Hk, dk_, **f32), torch.empty(T, Hk, dk_, **f32)
+        dvv, dg = torch.empty(T, H, dv_, **f32), torch.empty(T, H, **f32)
+        db = torch.empty(T, H, **f32)
+        dh0 = torch.empty(n_seq, H, dk_, dv_, **f32) if want_dh0 else None
     if workspace is None:
         workspace = _workspace(bwd_workspace_bytes(T, n_seq, Hk, H, dk_, dv_), dev)
     ins = [_Desc(t) for t in (q, k, v, g, beta)]
@@ -303,6 +316,79 @@ def chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor
         workspace.numel(), _stream(stream))
     nat.check(rc, "gdr_chunk_bwd")
     return dq, dkk, dvv, dg, db, dh0
+
+
+def _chunk_bwd_host_pipelined(q, k, v, g, beta, dout, scale, initial_state, cu_seqlens, dht,
+                              want_dh0, out, parts=_PIPE_PARTS, min_tokens=_PIPE_MIN_TOKENS):
+    """Host tensors: the backward of runs of whole segments on separate streams (copy in,
+    backward, copy out), as the forward's host path does; segments are independent, so
+    the gradients equal a single call's.  Gradients of tokens outside every segment are
+    zero.  Returns None when the call is too small or has a single run."""
+    T, Hk, dk = q.shape
+    H, dv = v.shape[1], v.shape[2]
+    if cu_seqlens is None or parts < 2 or T < min_tokens:
+        return None
+    if not all(t.is_pinned() for t in (q, k, v, g, beta, dout)):
+        return None
+    n_seq = cu_seqlens.numel() - 1
+    bounds = _segment_bounds(cu_seqlens.tolist(), T)
+    groups = _segment_groups(bounds, parts)
+    if len(groups) < 2:
+        return None
+    dev = torch.device("cuda", torch.cuda.current_device())
+    main = torch.cuda.current_stream(dev)
+    if scale is None:
+        scale = dk ** -0.5
+    shapes = [(T, Hk, dk), (T, Hk, dk), (T, H, dv), (T, H), (T, H), (n_seq, H, dk, dv)]
+    outs_h = list(out) if out is not None else [
+        torch.empty(sh, dtype=torch.float32, pin_memory=True) for sh in shapes]
+    if not want_dh0:
+        outs_h[5] = None
+    for t in outs_h[:5]:  # tokens outside every segment
+        t[:bounds[0]].zero_()
+        t[bounds[-1]:].zero_()
+    ins = {name: torch.empty(t.shape, dtype=t.dtype, device=dev)
+           for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("do", dout))}
+    outs_d = [torch.empty(sh, dtype=torch.float32, device=dev) for sh in shapes[:5]]
+    outs_d.append(torch.empty(shapes[5], dtype=torch.float32, device=dev) if want_dh0 else None)
+    h0_d = (torch.empty(initial_state.shape, dtype=initial_state.dtype, device=dev)
+            if initial_state is not None else None)
+    dht_d = torch.empty(dht.shape, dtype=dht.dtype, device=dev) if dht is not None else None
+    work = [_workspace(bwd_workspace_bytes(bounds[n1] - bounds[n0], n1 - n0, Hk, H, dk, dv), dev)
+            for n0, n1 in groups]
+    cus = [torch.tensor([b - bounds[n0] for b in bounds[n0:n1 + 1]], dtype=torch.int32)
+           .pin_memory() for n0, n1 in groups]
+    ready = torch.cuda.Event()
+    ready.record(main)
+    streams = [torch.cuda.Stream(dev) for _ in groups]
+    for (n0, n1), st, ws, cu_h in zip(groups, streams, work, cus):
+        st.wait_event(ready)
+        t0, t1 = bounds[n0], bounds[n1]
+        with torch.cuda.stream(st):
+            for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta),
+                            ("do", dout)):
+                ins[name][t0:t1].copy_(t[t0:t1], non_blocking=True)
+            cu_d = cu_h.to(dev, non_blocking=True)
+            h0g = dhtg = None
+            if h0_d is not None:
+                h0_d[n0:n1].copy_(initial_state[n0:n1], non_blocking=True)
+                h0g = h0_d[n0:n1]
+            if dht_d is not None:
+                dht_d[n0:n1].copy_(dht[n0:n1], non_blocking=True)
+                dhtg = dht_d[n0:n1]
+            og = tuple(o[t0:t1] for o in outs_d[:5]) + (
+                outs_d[5][n0:n1] if outs_d[5] is not None else None,)
+            chunk_bwd(ins["q"][t0:t1], ins["k"][t0:t1], ins["v"][t0:t1], ins["g"][t0:t1],
+                      ins["beta"][t0:t1], ins["do"][t0:t1], scale=scale, initial_state=h0g,
+                      cu_seqlens=cu_d, dht=dhtg, want_dh0=want_dh0, workspace=ws, stream=st,
+                      out=og)
+            for oh, od in zip(outs_h[:5], outs_d[:5]):
+                oh[t0:t1].copy_(od[t0:t1], non_blocking=True)
+            if want_dh0:
+                outs_h[5][n0:n1].copy_(outs_d[5][n0:n1], non_blocking=True)
+    for st in streams:
+        st.synchronize()
+    return tuple(outs_h)
 
 
 class _ChunkGatedDeltaRule(torch.autograd.Function):

@@ -220,3 +220,27 @@ def test_more_segments_than_a_grid_dimension_holds():
     ref = oracle.recurrent_bwd(w.q, w.k, w.v, w.g, w.beta, w.scale, None, w.cu_seqlens, do, None)
     for name, a, b in zip(NAMES[:5], got[:5], ref[:5]):
         _close(name, a, b, mask)
+
+
+@pytest.mark.parametrize("parts", [2, 4])
+def test_pipelined_host_backward_matches_device(parts):
+    # host tensors cut into runs of whole segments, one stream each: the gradients equal
+    # one device call's bit for bit, and tokens outside every segment get zeros
+    lens = [0, 500, 64, 0, 1200, 1, 700, 0]
+    w = make_workload("pipelined_bwd", 95, lens, 2, 4, 64, with_h0=True)
+    do, dht = _upstream(w, 96, True)
+    ref = _run_bwd(w, do, dht)
+    pin = lambda t: None if t is None else t.pin_memory()
+    # a few uncovered tokens after the last segment
+    extra = 5
+    padt = lambda t: torch.cat([t, torch.zeros((extra,) + tuple(t.shape[1:]), dtype=t.dtype)])
+    got = api._chunk_bwd_host_pipelined(
+        pin(padt(w.q)), pin(padt(w.k)), pin(padt(w.v)), pin(padt(w.g)), pin(padt(w.beta)),
+        pin(padt(do)), w.scale, pin(w.h0), w.cu_seqlens, pin(dht), True, None, parts=parts,
+        min_tokens=0)
+    for name, a, b in zip(NAMES, got, ref):
+        if name == "dh0":
+            assert torch.equal(a, b.cpu()), name
+        else:
+            assert torch.equal(a[:w.T], b.cpu()), name
+            assert not a[w.T:].any(), name
