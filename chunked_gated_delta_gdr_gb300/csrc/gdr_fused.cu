@@ -733,27 +733,26 @@ __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
       // once the previous chunk's MMAs that read them are done
       {
         const int ri = pid & 63, hc = (pid >> 6) * 32;
-        float v[32];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          float tq[4], bq[4];
-          ld_f4(AS + ri * kLdA + hc + q * 4, tq);
-          ld_f4(cv.beta + hc + q * 4, bq);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) v[q * 4 + u] = (hc + q * 4 + u <= ri) ? tq[u] * bq[u] : 0.f;
-        }
         if (g >= 1 && !wait_wg(sm, sm->vp_full, (g - 1) & 1, 0x305, kBarPrep)) { ok = false; break; }
+        // 8 columns at a time: a rolled loop keeps this block small in the instruction
+        // cache, which the SMs of a GPC share at full occupancy
+#pragma unroll 1
+        for (int q8 = 0; q8 < 32; q8 += 8) {
+          const int c0 = hc + q8;
+          float t8[8], b8[8], e8[8], v[8];
+          ld_f4(AS + ri * kLdA + c0, t8);
+          ld_f4(AS + ri * kLdA + c0 + 4, t8 + 4);
+          ld_f4(cv.beta + c0, b8);
+          ld_f4(cv.beta + c0 + 4, b8 + 4);
+          ld_f4(cv.eG + c0, e8);
+          ld_f4(cv.eG + c0 + 4, e8 + 4);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) store_chunk8(sbase + OFF_TB, ri, hc + q * 8, v + q * 8);
+          for (int u = 0; u < 8; ++u) v[u] = (c0 + u <= ri) ? t8[u] * b8[u] : 0.f;
+          store_chunk8(sbase + OFF_TB, ri, c0, v);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          float eq[4];
-          ld_f4(cv.eG + hc + q * 4, eq);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) v[q * 4 + u] *= -eq[u];
+          for (int u = 0; u < 8; ++u) v[u] *= -e8[u];
+          store_chunk8(sbase + OFF_TBG, ri, c0, v);
         }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) store_chunk8(sbase + OFF_TBG, ri, hc + q * 8, v + q * 8);
       }
       fence_async_smem();
       mbar_arrive(&sm->t_ready);
