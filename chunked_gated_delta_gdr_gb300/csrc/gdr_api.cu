@@ -164,8 +164,6 @@ size_t staged_bytes(int64_t T, int32_t n_seq, int32_t H, int32_t D) {
   return b;
 }
 
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
-
 FusedArgs fused_args(const Problem &P, float scale, void *work) {
   FusedArgs a{};
   a.T = P.T;

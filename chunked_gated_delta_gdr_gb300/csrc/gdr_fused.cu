@@ -190,20 +190,11 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                "r"(d));
 }
-__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t &a, uint32_t &b,
-                                             uint32_t &c, uint32_t &d) {
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
-               : "r"(addr));
-}
 
 __device__ __forceinline__ void zero_row(uint32_t tile, int row) {
 #pragma unroll
   for (int q = 0; q < 8; ++q) st_shared_v4(tile + row * 128 + q * 16, 0u, 0u, 0u, 0u);
 }
-
-__device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 
 // Fetch the next unit (segment, head) for this CTA into ring slot `slot`.
 __device__ void fetch_unit(const Params &p, Small *sm, int slot) {
