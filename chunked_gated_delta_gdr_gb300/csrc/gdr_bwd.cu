@@ -44,9 +44,10 @@ namespace {
 
 // ---------------------------------------------------------------- dV' intra part
 template <int D>
-struct DvIntraSmem {
-  static constexpr int kLd = ld_rows(D), kLdP = ld_cols(64);
-  static constexpr size_t bytes = sizeof(float) * (2 * 64 * kLd + 2 * 64 * kLdP + 64);
+struct DvIntraSmem {  // q, k, dO stay bf16 (as in memory)
+  static constexpr int kLd = ld_bf16(D), kLdD = ld_bf16(64), kLdP = ld_cols(64);
+  static constexpr size_t f32 = 64 * kLdP + 64;  // floats
+  static constexpr size_t bytes = sizeof(float) * f32 + sizeof(__nv_bfloat16) * (2 * 64 * kLd + 64 * kLdD);
 };
 
 template <int D>
@@ -55,16 +56,18 @@ __global__ void __launch_bounds__(kChunkThreads)
                    const ChunkInfo *__restrict__ chunks, const int32_t *__restrict__ n_chunks,
                    bool vec) {
   extern __shared__ float sm[];
-  constexpr int L = DvIntraSmem<D>::kLd, LP = DvIntraSmem<D>::kLdP;
+  constexpr int L = DvIntraSmem<D>::kLd, LD = DvIntraSmem<D>::kLdD, LP = DvIntraSmem<D>::kLdP;
   const int cid = blockIdx.x, h = blockIdx.y, cb = blockIdx.z * 64, tid = threadIdx.x;
   if (cid >= *n_chunks) return;
   const ChunkInfo ci = chunks[cid];
   const int len = ci.len, hk = h / group;
   const int64_t t0 = ci.start;
-  float *Qs = sm, *Ks = Qs + 64 * L, *Ds = Ks + 64 * L, *P = Ds + 64 * LP, *G = P + 64 * LP;
-  tile_bf16<64, D, kChunkThreads>(Qs, L, bf_row(q, t0, hk), q.st, len, vec);
-  tile_bf16<64, D, kChunkThreads>(Ks, L, bf_row(k, t0, hk), k.st, len, vec);
-  tile_bf16<64, 64, kChunkThreads>(Ds, LP, bf_row(dout, t0, h) + cb, dout.st, len, vec);
+  float *P = sm, *G = P + 64 * LP;
+  __nv_bfloat16 *Qs = reinterpret_cast<__nv_bfloat16 *>(sm + DvIntraSmem<D>::f32), *Ks = Qs + 64 * L,
+                *Ds = Ks + 64 * L;
+  tile_bf16_raw<64, D, kChunkThreads>(Qs, L, bf_row(q, t0, hk), q.st, len, vec);
+  tile_bf16_raw<64, D, kChunkThreads>(Ks, L, bf_row(k, t0, hk), k.st, len, vec);
+  tile_bf16_raw<64, 64, kChunkThreads>(Ds, LD, bf_row(dout, t0, h) + cb, dout.st, len, vec);
   if (tid < 64) G[tid] = tid < len ? ldf(gcum.p, (t0 + tid) * gcum.st + h * gcum.sh) : 0.f;
   __syncthreads();
   const int warp = tid >> 5;
@@ -72,7 +75,7 @@ __global__ void __launch_bounds__(kChunkThreads)
   {
     const int m0 = ((warp * kTPW) >> 3) * 16, nb = ((warp * kTPW) & 7) * 8;
     float accs[kTPW][4] = {};
-    mma_16xN<kTPW>(accs, SMat{Qs, L, 1}, m0, SMat{Ks, 1, L}, nb, 0, D);
+    mma_16xN<kTPW>(accs, SMatH{Qs, L, 1}, m0, SMatH{Ks, 1, L}, nb, 0, D);
 #pragma unroll
     for (int b = 0; b < kTPW; ++b) {
       const int n0 = nb + 8 * b;
@@ -90,7 +93,7 @@ __global__ void __launch_bounds__(kChunkThreads)
   {
     const int m0 = ((warp * kTPW) >> 3) * 16, nb = ((warp * kTPW) & 7) * 8;
     float accs[kTPW][4] = {};
-    mma_16xN<kTPW>(accs, SMat{P, 1, LP}, m0, SMat{Ds, LP, 1}, nb, 0, 64);
+    mma_16xN<kTPW>(accs, SMat{P, 1, LP}, m0, SMatH{Ds, LD, 1}, nb, 0, 64);
 #pragma unroll
     for (int b = 0; b < kTPW; ++b) {
       const int n0 = nb + 8 * b;
@@ -107,10 +110,11 @@ __global__ void __launch_bounds__(kChunkThreads)
 // ---------------------------------------------------------------- reverse state scan
 
 template <int D, int kScanCols>
-struct BwdScanSmem {
-  static constexpr int kLdK = ld_rows(D), kLdQ = ld_cols(D), kLdC = ld_cols(kScanCols);
+struct BwdScanSmem {  // K, W and Q stay bf16 (as in memory)
+  static constexpr int kLdK = ld_bf16(D), kLdQ = ld_bf16(D), kLdC = ld_cols(kScanCols);
+  static constexpr size_t f32 = D * kLdC + 2 * 64 * kLdC + 3 * 64;  // floats
   static constexpr size_t bytes =
-      sizeof(float) * (D * kLdC + 64 * kLdK + 2 * 64 * kLdQ + 2 * 64 * kLdC + 3 * 64);
+      sizeof(float) * f32 + sizeof(__nv_bfloat16) * (64 * kLdK + 2 * 64 * kLdQ);
 };
 
 // kScanCols value columns per block, kScanCols / 8 warps
@@ -130,8 +134,10 @@ __global__ void __launch_bounds__(kScanCols * 4)
   const int jb = (int)((bid / H) % Z) * kScanCols, tid = threadIdx.x;
   const int hk = h / group;
   const SegInfo si = seg[n];
-  float *dS = sm, *Ks = dS + D * LC, *Ws = Ks + 64 * LK, *Qs = Ws + 64 * LQ, *Dos = Qs + 64 * LQ;
-  float *Vd = Dos + 64 * LC, *G = Vd + 64 * LC, *Dec = G + 64, *EG = Dec + 64;
+  float *dS = sm, *Dos = dS + D * LC, *Vd = Dos + 64 * LC, *G = Vd + 64 * LC, *Dec = G + 64,
+        *EG = Dec + 64;
+  __nv_bfloat16 *Ks = reinterpret_cast<__nv_bfloat16 *>(sm + Sm::f32), *Ws = Ks + 64 * LK,
+                *Qs = Ws + 64 * LQ;
   const int64_t sbase = ((int64_t)n * H + h) * D * D;
   float *dvt = reinterpret_cast<float *>(dvp.p);
   for (int idx = tid; idx < D * kScanCols; idx += blockDim.x) {
@@ -148,9 +154,9 @@ __global__ void __launch_bounds__(kScanCols * 4)
       const int d = idx / kScanCols, j = idx % kScanCols;
       dhc[(int64_t)d * D + jb + j] = dS[d * LC + j];
     }
-    tile_bf16<64, D, NT>(Ks, LK, bf_row(k, t0, hk), k.st, len, vec);
-    tile_bf16<64, D, NT>(Ws, LQ, bf_row(w, t0, h), w.st, len, true);
-    tile_bf16<64, D, NT>(Qs, LQ, bf_row(q, t0, hk), q.st, len, vec);
+    tile_bf16_raw<64, D, NT>(Ks, LK, bf_row(k, t0, hk), k.st, len, vec);
+    tile_bf16_raw<64, D, NT>(Ws, LQ, bf_row(w, t0, h), w.st, len, true);
+    tile_bf16_raw<64, D, NT>(Qs, LQ, bf_row(q, t0, hk), q.st, len, vec);
     tile_bf16<64, kScanCols, NT>(Dos, LC, bf_row(dout, t0, h) + jb,
                                   dout.st, len, vec);
     tile_f32<64, kScanCols, NT>(Vd, LC, dvt + t0 * dvp.st + h * dvp.sh + jb, dvp.st, len);
@@ -169,7 +175,7 @@ __global__ void __launch_bounds__(kScanCols * 4)
     {
       const int m0 = ((warp * 4) / CT) * 16, nb = ((warp * 4) % CT) * 8;
       float accs[4][4] = {};
-      mma_16xN<4>(accs, SMat{Ks, LK, 1}, m0, SMat{dS, LC, 1}, nb, 0, D);
+      mma_16xN<4>(accs, SMatH{Ks, LK, 1}, m0, SMat{dS, LC, 1}, nb, 0, D);
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
         const int n0 = nb + 8 * b;
@@ -197,8 +203,8 @@ __global__ void __launch_bounds__(kScanCols * 4)
         constexpr int MB = D / 32;
         const int m0 = half * (D / 2);
         float inj[MB][4] = {}, corr[MB][4] = {};
-        mma_Mx8<MB>(inj, SMat{Qs, 1, LQ}, m0, SMat{Dos, LC, 1}, n0, 0, 64);
-        mma_Mx8<MB>(corr, SMat{Ws, 1, LQ}, m0, SMat{Vd, LC, 1}, n0, 0, 64);
+        mma_Mx8<MB>(inj, SMatH{Qs, 1, LQ}, m0, SMat{Dos, LC, 1}, n0, 0, 64);
+        mma_Mx8<MB>(corr, SMatH{Ws, 1, LQ}, m0, SMat{Vd, LC, 1}, n0, 0, 64);
 #pragma unroll
         for (int r = 0; r < MB; ++r)
 #pragma unroll
@@ -303,16 +309,17 @@ __global__ void __launch_bounds__(kChunkThreads)
 
 // ---------------------------------------------------------------- intra-chunk terms
 template <int D>
-struct IntraSmem {
-  static constexpr int kLd = ld_rows(D), kLdE = ld_rows(64);
-  static constexpr size_t bytes = sizeof(float) * (4 * 64 * kLd + 2 * 64 * kLdE + (3 + 2 * kQ) * 64);
+struct IntraSmem {  // q, k, dO, V' stay bf16 (as in memory): two blocks fit on an SM
+  static constexpr int kLd = ld_bf16(D), kLdE = ld_rows(64);
+  static constexpr size_t f32 = 2 * 64 * kLdE + (3 + 2 * kQ) * 64;  // floats
+  static constexpr size_t bytes = sizeof(float) * f32 + sizeof(__nv_bfloat16) * 4 * 64 * kLd;
 };
 
 // Warp w owns rows 16 (w % 4) .. +16 and column group w / 4 (of kQ) of the 64 x D
 // products; row sums go through a shuffle inside the tile, then kQ per-warp partials
 // added in a fixed order.
 template <int D>
-__global__ void __launch_bounds__(kChunkThreads)
+__global__ void __launch_bounds__(kChunkThreads, 2)
     k_bwd_intra(int32_t group, View q, View k, View dout, View v_new, View gcum, float scale,
                 View dqh, View dkh, float *dga, const ChunkInfo *__restrict__ chunks,
                 const int32_t *__restrict__ n_chunks, int32_t H, bool vec) {
@@ -323,14 +330,14 @@ __global__ void __launch_bounds__(kChunkThreads)
   const ChunkInfo ci = chunks[cid];
   const int len = ci.len, hk = h / group;
   const int64_t t0 = ci.start;
-  float *Qs = sm, *Ks = Qs + 64 * L, *Dos = Ks + 64 * L, *Vp = Dos + 64 * L;
-  float *E = Vp + 64 * L, *R = E + 64 * LE, *G = R + 64 * LE, *rowR = G + 64, *colR = rowR + 64;
+  float *E = sm, *R = E + 64 * LE, *G = R + 64 * LE, *rowR = G + 64, *colR = rowR + 64;
   float *aP = colR + 64, *cP = aP + kQ * 64;  // [kQ][64] partial row sums
-  tile_bf16<64, D, kChunkThreads>(Qs, L, bf_row(q, t0, hk), q.st, len, vec);
-  tile_bf16<64, D, kChunkThreads>(Ks, L, bf_row(k, t0, hk), k.st, len, vec);
-  tile_bf16<64, D, kChunkThreads>(Dos, L, bf_row(dout, t0, h), dout.st, len, vec);
-  tile_bf16<64, D, kChunkThreads>(Vp, L, bf_row(v_new, t0, h), v_new.st, len,
-                        true);
+  __nv_bfloat16 *Qs = reinterpret_cast<__nv_bfloat16 *>(sm + IntraSmem<D>::f32);
+  __nv_bfloat16 *Ks = Qs + 64 * L, *Dos = Ks + 64 * L, *Vp = Dos + 64 * L;
+  tile_bf16_raw<64, D, kChunkThreads>(Qs, L, bf_row(q, t0, hk), q.st, len, vec);
+  tile_bf16_raw<64, D, kChunkThreads>(Ks, L, bf_row(k, t0, hk), k.st, len, vec);
+  tile_bf16_raw<64, D, kChunkThreads>(Dos, L, bf_row(dout, t0, h), dout.st, len, vec);
+  tile_bf16_raw<64, D, kChunkThreads>(Vp, L, bf_row(v_new, t0, h), v_new.st, len, true);
   if (tid < 64) G[tid] = tid < len ? ldf(gcum.p, (t0 + tid) * gcum.st + h * gcum.sh) : 0.f;
   const int warp = tid >> 5;
   // this thread's elements of the dQ / dK accumulators (written by k_bwd_sgrad), loaded
@@ -352,8 +359,8 @@ __global__ void __launch_bounds__(kChunkThreads)
   {
     const int m0 = ((warp * kTPW) >> 3) * 16, nb = ((warp * kTPW) & 7) * 8;
     float dvs[kTPW][4] = {}, qks[kTPW][4] = {};
-    mma_16xN<kTPW>(dvs, SMat{Dos, L, 1}, m0, SMat{Vp, 1, L}, nb, 0, D);
-    mma_16xN<kTPW>(qks, SMat{Qs, L, 1}, m0, SMat{Ks, 1, L}, nb, 0, D);
+    mma_16xN<kTPW>(dvs, SMatH{Dos, L, 1}, m0, SMatH{Vp, 1, L}, nb, 0, D);
+    mma_16xN<kTPW>(qks, SMatH{Qs, L, 1}, m0, SMatH{Ks, 1, L}, nb, 0, D);
 #pragma unroll
     for (int b = 0; b < kTPW; ++b) {
       const int n0 = nb + 8 * b;
@@ -385,14 +392,14 @@ __global__ void __launch_bounds__(kChunkThreads)
   for (int c = 0; c < kCT; ++c) {
     const int n0 = (cg * kCT + c) * 8;
     float dq[4] = {0.f, 0.f, 0.f, 0.f}, dk[4] = {0.f, 0.f, 0.f, 0.f};
-    mma_16x8(dq, SMat{E, LE, 1}, m0, SMat{Ks, L, 1}, n0, 0, 64);
-    mma_16x8(dk, SMat{E, 1, LE}, m0, SMat{Qs, L, 1}, n0, 0, 64);
+    mma_16x8(dq, SMat{E, LE, 1}, m0, SMatH{Ks, L, 1}, n0, 0, 64);
+    mma_16x8(dk, SMat{E, 1, LE}, m0, SMatH{Qs, L, 1}, n0, 0, 64);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int i = acc_row(m0, e), d = acc_col(n0, e);
       if (i < len) {
-        ap[e >> 1] += Qs[i * L + d] * qpre[c][e];
-        cp[e >> 1] += Ks[i * L + d] * kpre[c][e];
+        ap[e >> 1] += __bfloat162float(Qs[i * L + d]) * qpre[c][e];
+        cp[e >> 1] += __bfloat162float(Ks[i * L + d]) * kpre[c][e];
         q_out[(t0 + i) * dqh.st + h * dqh.sh + d] = qpre[c][e] + dq[e];
         k_out[(t0 + i) * dkh.st + h * dkh.sh + d] = kpre[c][e] + dk[e];
       }
@@ -745,8 +752,11 @@ cudaError_t launch_bwd_d(const BwdArgs &a, const BwdWs &w, cudaStream_t stream) 
                                                        a.order, vec);
     return cudaGetLastError();
   };
-  e = scan_cols(s.n_seq, s.H, D) == 64 ? scan(k_bwd_scan<D, 64>, 64, BwdScanSmem<D, 64>::bytes)
-                                       : scan(k_bwd_scan<D, 32>, 32, BwdScanSmem<D, 32>::bytes);
+  // at d = 128 the 32-column blocks (bf16 operand tiles, 94 KB) fit two to an SM and ran
+  // faster than 64-column blocks at one per SM
+  const int bcols = D == 128 ? 32 : scan_cols(s.n_seq, s.H, D);
+  e = bcols == 64 ? scan(k_bwd_scan<D, 64>, 64, BwdScanSmem<D, 64>::bytes)
+                  : scan(k_bwd_scan<D, 32>, 32, BwdScanSmem<D, 32>::bytes);
   if (e != cudaSuccess) return e;
   if ((e = set_smem(k_bwd_sgrad<D>, SgradSmem<D>::bytes)) != cudaSuccess) return e;
   k_bwd_sgrad<D><<<dim3(gc.x, gc.y, D / kSRows), kChunkThreads, SgradSmem<D>::bytes, stream>>>(

@@ -41,22 +41,34 @@ struct SMat {
   const float *p;
   int rs, cs;
 };
+// The same for a bf16 matrix (an operand whose values came from a bf16 tensor: it takes
+// half the shared memory, and every bf16 value is exactly a tf32 value).
+struct SMatH {
+  const __nv_bfloat16 *p;
+  int rs, cs;
+};
+// Element i of a view as a tf32 operand.
+__device__ __forceinline__ uint32_t tf32_at(const SMat &m, int i) { return tf32_rn(m.p[i]); }
+__device__ __forceinline__ uint32_t tf32_at(const SMatH &m, int i) {
+  return (uint32_t)reinterpret_cast<const uint16_t *>(m.p)[i] << 16;
+}
 
 // One warp: acc[16 x 8] += A[m0 .. m0+16, k0 .. k1) * B[k0 .. k1, n0 .. n0+8), with
 // k1 - k0 a multiple of 8.  Accumulator element e (0..3) of lane l holds
 // (m0 + l/4 + 8 (e/2), n0 + 2 (l%4) + e%2).
-__device__ __forceinline__ void mma_16x8(float (&acc)[4], SMat A, int m0, SMat B, int n0, int k0,
+template <class VA, class VB>
+__device__ __forceinline__ void mma_16x8(float (&acc)[4], VA A, int m0, VB B, int n0, int k0,
                                          int k1) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const float *ab = A.p + (m0 + g) * A.rs;
-  const float *bb = B.p + (n0 + g) * B.cs;
+  const int ab = (m0 + g) * A.rs;
+  const int bb = (n0 + g) * B.cs;
 #pragma unroll 2
   for (int k = k0; k < k1; k += 8) {
-    const float *ap = ab + (k + t) * A.cs;
-    const float *bp = bb + (k + t) * B.rs;
-    const uint32_t a0 = tf32_rn(ap[0]), a1 = tf32_rn(ap[8 * A.rs]);
-    const uint32_t a2 = tf32_rn(ap[4 * A.cs]), a3 = tf32_rn(ap[8 * A.rs + 4 * A.cs]);
-    const uint32_t b0 = tf32_rn(bp[0]), b1 = tf32_rn(bp[4 * B.rs]);
+    const int ap = ab + (k + t) * A.cs;
+    const int bp = bb + (k + t) * B.rs;
+    const uint32_t a0 = tf32_at(A, ap), a1 = tf32_at(A, ap + 8 * A.rs);
+    const uint32_t a2 = tf32_at(A, ap + 4 * A.cs), a3 = tf32_at(A, ap + 8 * A.rs + 4 * A.cs);
+    const uint32_t b0 = tf32_at(B, bp), b1 = tf32_at(B, bp + 4 * B.rs);
     asm volatile(
         "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
         "{%8,%9}, {%0,%1,%2,%3};"
@@ -68,20 +80,20 @@ __device__ __forceinline__ void mma_16x8(float (&acc)[4], SMat A, int m0, SMat B
 // One warp: NB adjacent tiles, acc[b][16 x 8] += A[m0.., k] B[k, n0 + 8 b ..]; the A
 // fragment is loaded once per k step and the NB products are independent, so their
 // latencies overlap.
-template <int NB>
-__device__ __forceinline__ void mma_16xN(float (&acc)[NB][4], SMat A, int m0, SMat B, int n0,
+template <int NB, class VA, class VB>
+__device__ __forceinline__ void mma_16xN(float (&acc)[NB][4], VA A, int m0, VB B, int n0,
                                          int k0, int k1) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const float *ab = A.p + (m0 + g) * A.rs;
+  const int ab = (m0 + g) * A.rs;
 #pragma unroll 2
   for (int k = k0; k < k1; k += 8) {
-    const float *ap = ab + (k + t) * A.cs;
-    const uint32_t a0 = tf32_rn(ap[0]), a1 = tf32_rn(ap[8 * A.rs]);
-    const uint32_t a2 = tf32_rn(ap[4 * A.cs]), a3 = tf32_rn(ap[8 * A.rs + 4 * A.cs]);
+    const int ap = ab + (k + t) * A.cs;
+    const uint32_t a0 = tf32_at(A, ap), a1 = tf32_at(A, ap + 8 * A.rs);
+    const uint32_t a2 = tf32_at(A, ap + 4 * A.cs), a3 = tf32_at(A, ap + 8 * A.rs + 4 * A.cs);
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
-      const float *bp = B.p + (n0 + 8 * b + g) * B.cs + (k + t) * B.rs;
-      const uint32_t b0 = tf32_rn(bp[0]), b1 = tf32_rn(bp[4 * B.rs]);
+      const int bp = (n0 + 8 * b + g) * B.cs + (k + t) * B.rs;
+      const uint32_t b0 = tf32_at(B, bp), b1 = tf32_at(B, bp + 4 * B.rs);
       asm volatile(
           "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
           "{%8,%9}, {%0,%1,%2,%3};"
@@ -93,20 +105,20 @@ __device__ __forceinline__ void mma_16xN(float (&acc)[NB][4], SMat A, int m0, SM
 
 // One warp: MB row tiles (m0 + 16 r) sharing one column tile (n0); the B fragment is
 // loaded once per k step and the MB products are independent.
-template <int MB>
-__device__ __forceinline__ void mma_Mx8(float (&acc)[MB][4], SMat A, int m0, SMat B, int n0,
+template <int MB, class VA, class VB>
+__device__ __forceinline__ void mma_Mx8(float (&acc)[MB][4], VA A, int m0, VB B, int n0,
                                         int k0, int k1) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const float *bb = B.p + (n0 + g) * B.cs;
+  const int bb = (n0 + g) * B.cs;
 #pragma unroll 2
   for (int k = k0; k < k1; k += 8) {
-    const float *bp = bb + (k + t) * B.rs;
-    const uint32_t b0 = tf32_rn(bp[0]), b1 = tf32_rn(bp[4 * B.rs]);
+    const int bp = bb + (k + t) * B.rs;
+    const uint32_t b0 = tf32_at(B, bp), b1 = tf32_at(B, bp + 4 * B.rs);
 #pragma unroll
     for (int r = 0; r < MB; ++r) {
-      const float *ap = A.p + (m0 + 16 * r + g) * A.rs + (k + t) * A.cs;
-      const uint32_t a0 = tf32_rn(ap[0]), a1 = tf32_rn(ap[8 * A.rs]);
-      const uint32_t a2 = tf32_rn(ap[4 * A.cs]), a3 = tf32_rn(ap[8 * A.rs + 4 * A.cs]);
+      const int ap = (m0 + 16 * r + g) * A.rs + (k + t) * A.cs;
+      const uint32_t a0 = tf32_at(A, ap), a1 = tf32_at(A, ap + 8 * A.rs);
+      const uint32_t a2 = tf32_at(A, ap + 4 * A.cs), a3 = tf32_at(A, ap + 8 * A.rs + 4 * A.cs);
       asm volatile(
           "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
           "{%8,%9}, {%0,%1,%2,%3};"
@@ -131,6 +143,9 @@ constexpr int kChunkThreads = 512, kWarps = kChunkThreads / 32, kTPW = 32 / kWar
 // operand in 32 different banks, a stride of 8 mod 32 those of a transposed one.
 __host__ __device__ constexpr int ld_rows(int cols) { return cols + 4; }   // read as rows
 __host__ __device__ constexpr int ld_cols(int cols) { return cols + 8; }   // read transposed
+// bf16 operands: a word holds two neighbours, so with a stride of 8 mod 64 elements both
+// reads map a warp's 32 lanes onto 16 different words (lanes sharing a word get it at once).
+__host__ __device__ constexpr int ld_bf16(int cols) { return cols + 8; }
 constexpr int kLdY = 24;  // 16 x 16 scratch tiles of the solve (read as the B operand)
 constexpr int kSolveScratch = 8 * 16 * kLdY;
 
@@ -234,6 +249,38 @@ __device__ __forceinline__ void tile_bf16(float *dst, int ld, const __nv_bfloat1
     for (int idx = threadIdx.x; idx < R * C; idx += NT) {
       const int r = idx / C, c = idx % C;
       dst[r * ld + c] = r < len ? __bfloat162float(src[r * rs + c]) : 0.f;
+    }
+  }
+}
+
+// As tile_bf16, into bf16 shared memory as it is (dst 16-byte aligned, ld a multiple of 8).
+template <int R, int C, int NT>
+__device__ __forceinline__ void tile_bf16_raw(__nv_bfloat16 *dst, int ld, const __nv_bfloat16 *src,
+                                              int64_t rs, int len, bool vec) {
+  constexpr int VPR = C / 8, NV = R * VPR;
+  static_assert(C % 8 == 0 && NV % NT == 0, "tile shape");
+  constexpr int PER = NV / NT, BATCH = PER < 8 ? PER : 8;
+  static_assert(PER % BATCH == 0, "whole batches");
+  if (vec) {
+#pragma unroll
+    for (int b0 = 0; b0 < PER; b0 += BATCH) {
+      uint4 x[BATCH];
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u) {
+        const int v = threadIdx.x + (b0 + u) * NT, r = v / VPR, c = (v % VPR) * 8;
+        x[u] = r < len ? *reinterpret_cast<const uint4 *>(src + r * rs + c) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u) {
+        const int v = threadIdx.x + (b0 + u) * NT, r = v / VPR, c = (v % VPR) * 8;
+        *reinterpret_cast<uint4 *>(dst + r * ld + c) = x[u];
+      }
+    }
+  } else {
+    const __nv_bfloat16 zero = __float2bfloat16(0.f);
+    for (int idx = threadIdx.x; idx < R * C; idx += NT) {
+      const int r = idx / C, c = idx % C;
+      dst[r * ld + c] = r < len ? src[r * rs + c] : zero;
     }
   }
 }

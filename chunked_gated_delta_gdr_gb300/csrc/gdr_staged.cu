@@ -20,15 +20,17 @@ namespace gdr {
 namespace {
 
 // ---------------------------------------------------------------- stage 1
+// K and V stay bf16 in shared memory (half the bytes of fp32 tiles, the same operand
+// values): two blocks fit on an SM, so one block's loads overlap another's products.
 template <int D>
 struct PrepSmem {
-  static constexpr int kLd = ld_rows(D), kLdA = ld_rows(64);
-  static constexpr size_t bytes =
-      sizeof(float) * (2 * 64 * kLd + 3 * 64 * kLdA + 3 * 64 + kSolveScratch);
+  static constexpr int kLd = ld_bf16(D), kLdA = ld_rows(64);
+  static constexpr size_t f32 = 3 * 64 * kLdA + 3 * 64 + kSolveScratch;  // floats
+  static constexpr size_t bytes = sizeof(float) * f32 + sizeof(__nv_bfloat16) * 2 * 64 * kLd;
 };
 
 template <int D>
-__global__ void __launch_bounds__(kChunkThreads)
+__global__ void __launch_bounds__(kChunkThreads, 2)
     k_prep(int32_t group, View k, View v, View g, View beta, View w, View u, View gcum,
            const ChunkInfo *__restrict__ chunks, const int32_t *__restrict__ n_chunks, bool vec) {
   extern __shared__ float sm[];
@@ -38,11 +40,12 @@ __global__ void __launch_bounds__(kChunkThreads)
   const ChunkInfo ci = chunks[cid];
   const int len = ci.len, hk = h / group;
   const int64_t t0 = ci.start;
-  float *Ks = sm, *Vs = Ks + 64 * L, *Am = Vs + 64 * L, *Tm = Am + 64 * LA, *TU = Tm + 64 * LA;
+  float *Am = sm, *Tm = Am + 64 * LA, *TU = Tm + 64 * LA;
   float *G = TU + 64 * LA, *B = G + 64, *BG = B + 64, *scratch = BG + 64;
+  __nv_bfloat16 *Ks = reinterpret_cast<__nv_bfloat16 *>(sm + PrepSmem<D>::f32), *Vs = Ks + 64 * L;
 
-  tile_bf16<64, D, kChunkThreads>(Ks, L, bf_row(k, t0, hk), k.st, len, vec);
-  tile_bf16<64, D, kChunkThreads>(Vs, L, bf_row(v, t0, h), v.st, len, vec);
+  tile_bf16_raw<64, D, kChunkThreads>(Ks, L, bf_row(k, t0, hk), k.st, len, vec);
+  tile_bf16_raw<64, D, kChunkThreads>(Vs, L, bf_row(v, t0, h), v.st, len, vec);
   if (tid < 64) {
     G[tid] = tid < len ? ldf(g.p, (t0 + tid) * g.st + h * g.sh) : 0.f;
     B[tid] = tid < len ? ldbf(beta.p, (t0 + tid) * beta.st + h * beta.sh) : 0.f;
@@ -67,7 +70,7 @@ __global__ void __launch_bounds__(kChunkThreads)
   {
     const int m0 = ((warp * kTPW) >> 3) * 16, nb = ((warp * kTPW) & 7) * 8;
     float accs[kTPW][4] = {};
-    mma_16xN<kTPW>(accs, SMat{Ks, L, 1}, m0, SMat{Ks, 1, L}, nb, 0, D);
+    mma_16xN<kTPW>(accs, SMatH{Ks, L, 1}, m0, SMatH{Ks, 1, L}, nb, 0, D);
 #pragma unroll
     for (int b = 0; b < kTPW; ++b) {
       const int n0 = nb + 8 * b;
@@ -92,8 +95,8 @@ __global__ void __launch_bounds__(kChunkThreads)
   for (int tl = warp; tl < 4 * (D / 8); tl += kWarps) {
     const int m0 = (tl & 3) * 16, n0 = (tl >> 2) * 8;
     float wa[4] = {0.f, 0.f, 0.f, 0.f}, ua[4] = {0.f, 0.f, 0.f, 0.f};
-    mma_16x8(wa, SMat{Am, LA, 1}, m0, SMat{Ks, L, 1}, n0, 0, 64);
-    mma_16x8(ua, SMat{TU, LA, 1}, m0, SMat{Vs, L, 1}, n0, 0, 64);
+    mma_16x8(wa, SMat{Am, LA, 1}, m0, SMatH{Ks, L, 1}, n0, 0, 64);
+    mma_16x8(ua, SMat{TU, LA, 1}, m0, SMatH{Vs, L, 1}, n0, 0, 64);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int i = acc_row(m0, e), d = acc_col(n0, e);
@@ -108,22 +111,25 @@ __global__ void __launch_bounds__(kChunkThreads)
 
 // ---------------------------------------------------------------- stage 2
 
+// W, K and U stay bf16 in shared memory (as stored): two blocks fit on an SM.
 template <int D, int kScanCols>
 struct ScanSmem {
-  static constexpr int kLdW = ld_rows(D), kLdK = ld_cols(D), kLdC = ld_cols(kScanCols);
+  static constexpr int kLdW = ld_bf16(D), kLdK = ld_bf16(D), kLdU = ld_bf16(kScanCols),
+                       kLdC = ld_cols(kScanCols);
+  static constexpr size_t f32 = D * kLdC + 64 * kLdC + 2 * 64;  // floats
   static constexpr size_t bytes =
-      sizeof(float) * (D * kLdC + 64 * kLdW + 64 * kLdK + 2 * 64 * kLdC + 2 * 64);
+      sizeof(float) * f32 + sizeof(__nv_bfloat16) * (64 * kLdW + 64 * kLdK + 64 * kLdU);
 };
 
 // kScanCols value columns per block, kScanCols / 8 warps
 template <int D, int kScanCols>
-__global__ void __launch_bounds__(kScanCols * 4)
+__global__ void __launch_bounds__(kScanCols * 4, 2)
     k_scan(int32_t H, int32_t group, View k, View w, View u, View gcum, const float *h0,
            __nv_bfloat16 *hbuf, View v_new, float *ht, Ckpt ck,
            const SegInfo *__restrict__ seg, const int32_t *__restrict__ order, bool vec) {
   extern __shared__ float sm[];
   using Sm = ScanSmem<D, kScanCols>;
-  constexpr int LW = Sm::kLdW, LK = Sm::kLdK, LC = Sm::kLdC;
+  constexpr int LW = Sm::kLdW, LK = Sm::kLdK, LU = Sm::kLdU, LC = Sm::kLdC;
   constexpr int NT = kScanCols * 4, NW = kScanCols / 8, CT = kScanCols / 8;  // threads, warps, column tiles
   // one flat grid, head fastest, then column block, then segment rank: the longest
   // segments are dispatched first (a flat x extent allows any segment count)
@@ -133,8 +139,9 @@ __global__ void __launch_bounds__(kScanCols * 4)
   const int jb = (int)((bid / H) % Z) * kScanCols, tid = threadIdx.x;
   const int hk = h / group;
   const SegInfo si = seg[n];
-  float *S = sm, *Ws = S + D * LC, *Ks = Ws + 64 * LW, *Us = Ks + 64 * LK, *Vn = Us + 64 * LC;
-  float *G = Vn + 64 * LC, *Dec = G + 64;
+  float *S = sm, *Vn = S + D * LC, *G = Vn + 64 * LC, *Dec = G + 64;
+  __nv_bfloat16 *Ws = reinterpret_cast<__nv_bfloat16 *>(sm + Sm::f32), *Ks = Ws + 64 * LW,
+                *Us = Ks + 64 * LK;
   const int64_t sbase = ((int64_t)n * H + h) * D * D;
 
   for (int idx = tid; idx < D * kScanCols; idx += blockDim.x) {
@@ -162,12 +169,9 @@ __global__ void __launch_bounds__(kScanCols * 4)
       const int d = idx / kScanCols, j = idx % kScanCols;
       hc[(int64_t)d * D + jb + j] = __float2bfloat16_rn(S[d * LC + j]);
     }
-    tile_bf16<64, D, NT>(Ws, LW, bf_row(w, t0, h),
-                          w.st, len, vec);
-    tile_bf16<64, D, NT>(Ks, LK, bf_row(k, t0, hk), k.st, len, vec);
-    tile_bf16<64, kScanCols, NT>(
-        Us, LC, bf_row(u, t0, h) + jb, u.st, len,
-        vec);
+    tile_bf16_raw<64, D, NT>(Ws, LW, bf_row(w, t0, h), w.st, len, vec);
+    tile_bf16_raw<64, D, NT>(Ks, LK, bf_row(k, t0, hk), k.st, len, vec);
+    tile_bf16_raw<64, kScanCols, NT>(Us, LU, bf_row(u, t0, h) + jb, u.st, len, vec);
     if (tid < 64) G[tid] = tid < len ? ldf(gcum.p, (t0 + tid) * gcum.st + h * gcum.sh) : 0.f;
     __syncthreads();
     const float glast = G[len - 1];
@@ -179,7 +183,7 @@ __global__ void __launch_bounds__(kScanCols * 4)
     {
       const int m0 = ((warp * 4) / CT) * 16, nb = ((warp * 4) % CT) * 8;
       float accs[4][4] = {};
-      mma_16xN<4>(accs, SMat{Ws, LW, 1}, m0, SMat{S, LC, 1}, nb, 0, D);
+      mma_16xN<4>(accs, SMatH{Ws, LW, 1}, m0, SMat{S, LC, 1}, nb, 0, D);
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
         const int n0 = nb + 8 * b;
@@ -189,7 +193,7 @@ __global__ void __launch_bounds__(kScanCols * 4)
           const int i = acc_row(m0, e), j = acc_col(n0, e);
           float vn = 0.f;
           if (i < len) {
-            const __nv_bfloat16 b = __float2bfloat16_rn(Us[i * LC + j] - acc[e]);
+            const __nv_bfloat16 b = __float2bfloat16_rn(__bfloat162float(Us[i * LU + j]) - acc[e]);
             reinterpret_cast<__nv_bfloat16 *>(v_new.p)[(t0 + i) * v_new.st + h * v_new.sh + jb + j] = b;
             vn = Dec[i] * __bfloat162float(b);
           }
@@ -206,7 +210,7 @@ __global__ void __launch_bounds__(kScanCols * 4)
       constexpr int MB = D / 16;
       const int n0 = warp * 8;
       float acc[MB][4] = {};
-      mma_Mx8<MB>(acc, SMat{Ks, 1, LK}, 0, SMat{Vn, LC, 1}, n0, 0, 64);
+      mma_Mx8<MB>(acc, SMatH{Ks, 1, LK}, 0, SMat{Vn, LC, 1}, n0, 0, 64);
 #pragma unroll
       for (int r = 0; r < MB; ++r)
 #pragma unroll
@@ -230,57 +234,74 @@ __global__ void __launch_bounds__(kScanCols * 4)
 // ---------------------------------------------------------------- stage 3
 constexpr int kOutCols = 64;
 
+// q, k, h and V' stay bf16 in shared memory (as in memory); P is fp32.
 template <int D>
 struct OutSmem {
-  static constexpr int kLd = ld_rows(D), kLdH = ld_rows(kOutCols);
+  static constexpr int kLd = ld_bf16(D), kLdH = ld_bf16(kOutCols), kLdP = ld_rows(64);
+  static constexpr size_t f32 = 64 * kLdP + 2 * 64;  // floats
   static constexpr size_t bytes =
-      sizeof(float) * (2 * 64 * kLd + D * kLdH + 64 * kLdH + 64 * 65 + 64);
+      sizeof(float) * f32 + sizeof(__nv_bfloat16) * (2 * 64 * kLd + D * kLdH + 64 * kLdH);
 };
 
+// Block (chunk, head, column block of kOutCols value columns), 8 warps: every product is
+// a set of tensor-core tiles, four 16 x 8 tiles per warp.
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 2)
     k_out(int32_t H, int32_t group, View q, View k, View v_new, const __nv_bfloat16 *hbuf,
           View gcum, float scale, View o, const ChunkInfo *__restrict__ chunks,
           const int32_t *__restrict__ n_chunks, bool vec) {
   extern __shared__ float sm[];
-  constexpr int L = OutSmem<D>::kLd, LH = OutSmem<D>::kLdH;
+  using Sm = OutSmem<D>;
+  constexpr int L = Sm::kLd, LH = Sm::kLdH, LP = Sm::kLdP;
   const int cid = blockIdx.x, h = blockIdx.y, cb = blockIdx.z * kOutCols, tid = threadIdx.x;
   if (cid >= *n_chunks) return;
   const ChunkInfo ci = chunks[cid];
   const int len = ci.len, hk = h / group;
   const int64_t t0 = ci.start;
-  float *Qs = sm, *Ks = Qs + 64 * L, *Hs = Ks + 64 * L, *Vn = Hs + D * LH, *P = Vn + 64 * LH;
-  float *G = P + 64 * 65;
+  float *P = sm, *G = P + 64 * LP, *EG = G + 64;
+  __nv_bfloat16 *Qs = reinterpret_cast<__nv_bfloat16 *>(sm + Sm::f32), *Ks = Qs + 64 * L,
+                *Hs = Ks + 64 * L, *Vn = Hs + D * LH;
 
-  tile_bf16<64, D, 256>(Qs, L, bf_row(q, t0, hk), q.st, len, vec);
-  tile_bf16<64, D, 256>(Ks, L, bf_row(k, t0, hk), k.st, len, vec);
+  tile_bf16_raw<64, D, 256>(Qs, L, bf_row(q, t0, hk), q.st, len, vec);
+  tile_bf16_raw<64, D, 256>(Ks, L, bf_row(k, t0, hk), k.st, len, vec);
   const __nv_bfloat16 *hc = hbuf + ((int64_t)cid * H + h) * D * D;
-  tile_bf16<D, kOutCols, 256>(Hs, LH, hc + cb, D, D, vec);
-  tile_bf16<64, kOutCols, 256>(Vn, LH, bf_row(v_new, t0, h) + cb,
-                               v_new.st, len, vec);
-  if (tid < 64) G[tid] = tid < len ? ldf(gcum.p, (t0 + tid) * gcum.st + h * gcum.sh) : 0.f;
-  __syncthreads();
-  for (int idx = tid; idx < 64 * 64; idx += blockDim.x) {
-    const int i = idx / 64, j = idx % 64;
-    float pv = 0.f;
-    if (j <= i && i < len) {
-      float dot = 0.f;
-#pragma unroll 8
-      for (int d = 0; d < D; ++d) dot += Qs[i * L + d] * Ks[j * L + d];
-      pv = expf(G[i] - G[j]) * dot;
-    }
-    P[i * 65 + j] = pv;
+  tile_bf16_raw<D, kOutCols, 256>(Hs, LH, hc + cb, D, D, vec);
+  tile_bf16_raw<64, kOutCols, 256>(Vn, LH, bf_row(v_new, t0, h) + cb, v_new.st, len, vec);
+  if (tid < 64) {
+    const float gi = tid < len ? ldf(gcum.p, (t0 + tid) * gcum.st + h * gcum.sh) : 0.f;
+    G[tid] = gi;
+    EG[tid] = tid < len ? expf(gi) : 0.f;
   }
   __syncthreads();
-  for (int idx = tid; idx < 64 * kOutCols; idx += blockDim.x) {
-    const int i = idx / kOutCols, c = idx % kOutCols;
-    if (i >= len) continue;
-    float inter = 0.f, intra = 0.f;
-#pragma unroll 8
-    for (int d = 0; d < D; ++d) inter += Qs[i * L + d] * Hs[d * LH + c];
-    for (int j = 0; j <= i; ++j) intra += P[i * 65 + j] * Vn[j * LH + c];
-    const float r = scale * (expf(G[i]) * inter + intra);
-    stbf(o.p, (t0 + i) * o.st + h * o.sh + cb + c, r);
+  const int warp = tid >> 5;
+  const int m0 = ((warp * 4) >> 3) * 16, nb = ((warp * 4) & 7) * 8;  // 16 rows x 32 columns
+  // P = tril(Gam) o (Q K^T), Gam_ij = e^{G_i - G_j}
+  {
+    float accs[4][4] = {};
+    mma_16xN<4>(accs, SMatH{Qs, L, 1}, m0, SMatH{Ks, 1, L}, nb, 0, D);
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = acc_row(m0, e), j = acc_col(nb + 8 * b, e);
+        P[i * LP + j] = (j <= i && i < len) ? expf(G[i] - G[j]) * accs[b][e] : 0.f;
+      }
+  }
+  __syncthreads();
+  // O[:, cb ..] = scale (diag(e^G) Q h + P V')
+  {
+    float inter[4][4] = {}, intra[4][4] = {};
+    mma_16xN<4>(inter, SMatH{Qs, L, 1}, m0, SMatH{Hs, LH, 1}, nb, 0, D);
+    mma_16xN<4>(intra, SMat{P, LP, 1}, m0, SMatH{Vn, LH, 1}, nb, 0, 64);
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = acc_row(m0, e), c = acc_col(nb + 8 * b, e);
+        if (i < len)
+          stbf(o.p, (t0 + i) * o.st + h * o.sh + cb + c,
+               scale * (EG[i] * inter[b][e] + intra[b][e]));
+      }
   }
 }
 
