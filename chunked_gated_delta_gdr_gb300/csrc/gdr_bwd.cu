@@ -227,77 +227,81 @@ __global__ void __launch_bounds__(kScanCols * 4)
 // ---------------------------------------------------------------- products with S_0, dS_C
 constexpr int kSRows = 64;  // key rows of S_0 / dS_C per block
 
-template <int D>
+// The products reduce over the value dimension, taken 64 columns at a time: per pass
+// S_0, dO, V' as bf16 (their values are bf16) and dS_C, dV' as fp32, 65 KB, so two
+// blocks fit on an SM.
+constexpr int kSCols = 64;
 struct SgradSmem {
-  static constexpr int kLd = ld_rows(D);
+  static constexpr int kLdB = ld_bf16(kSCols), kLdF = ld_rows(kSCols);
+  static constexpr size_t f32 = (kSRows + 64) * kLdF + 2 * 64 + kChunkThreads;  // floats
   static constexpr size_t bytes =
-      sizeof(float) * (2 * kSRows * kLd + 3 * 64 * kLd + 2 * 64 + kChunkThreads);
+      sizeof(float) * f32 + sizeof(__nv_bfloat16) * (kSRows + 2 * 64) * kLdB;
 };
 
 template <int D>
-__global__ void __launch_bounds__(kChunkThreads)
+__global__ void __launch_bounds__(kChunkThreads, 2)
     k_bwd_sgrad(View dout, View v_new, View gcum, float scale, const __nv_bfloat16 *hbuf,
                 const float *dh, View dvp, View dqh, View dkh, View dw, float *sdot,
                 const ChunkInfo *__restrict__ chunks, const int32_t *__restrict__ n_chunks,
                 int32_t H, bool vec) {
   extern __shared__ float sm[];
-  constexpr int L = SgradSmem<D>::kLd;
+  constexpr int LB = SgradSmem::kLdB, LF = SgradSmem::kLdF;
   const int cid = blockIdx.x, h = blockIdx.y, rb = blockIdx.z * kSRows, tid = threadIdx.x;
   if (cid >= *n_chunks) return;
   const ChunkInfo ci = chunks[cid];
   const int len = ci.len;
   const int64_t t0 = ci.start;
-  float *S0 = sm, *dS = S0 + kSRows * L, *Dos = dS + kSRows * L, *Vp = Dos + 64 * L;
-  float *dV = Vp + 64 * L, *Dec = dV + 64 * L, *EG = Dec + 64, *red = EG + 64;
-  const __nv_bfloat16 *hc = hbuf + ((int64_t)cid * H + h) * D * D;
-  const float *dhc = dh + ((int64_t)cid * H + h) * D * D;
-  tile_bf16<kSRows, D, kChunkThreads>(S0, L, hc + (int64_t)rb * D, D, kSRows, true);
-  tile_f32<kSRows, D, kChunkThreads>(dS, L, dhc + (int64_t)rb * D, D, kSRows);
-  const float *dvt = reinterpret_cast<const float *>(dvp.p);
-  tile_bf16<64, D, kChunkThreads>(Dos, L, bf_row(dout, t0, h), dout.st, len, vec);
-  tile_bf16<64, D, kChunkThreads>(Vp, L, bf_row(v_new, t0, h), v_new.st, len,
-                        true);
-  tile_f32<64, D, kChunkThreads>(dV, L, dvt + t0 * dvp.st + h * dvp.sh, dvp.st, len);
+  float *dS = sm, *dV = dS + kSRows * LF, *Dec = dV + 64 * LF, *EG = Dec + 64, *red = EG + 64;
+  __nv_bfloat16 *S0 = reinterpret_cast<__nv_bfloat16 *>(sm + SgradSmem::f32);
+  __nv_bfloat16 *Dos = S0 + kSRows * LB, *Vp = Dos + 64 * LB;
+  const __nv_bfloat16 *hc = hbuf + ((int64_t)cid * H + h) * D * D + (int64_t)rb * D;
+  const float *dhc = dh + ((int64_t)cid * H + h) * D * D + (int64_t)rb * D;
+  const float *dvt = reinterpret_cast<const float *>(dvp.p) + t0 * dvp.st + h * dvp.sh;
   if (tid < 64) {
     const float gi = tid < len ? ldf(gcum.p, (t0 + tid) * gcum.st + h * gcum.sh) : 0.f;
     const float gl = ldf(gcum.p, (t0 + len - 1) * gcum.st + h * gcum.sh);
     Dec[tid] = tid < len ? expf(gl - gi) : 0.f;
     EG[tid] = tid < len ? expf(gi) : 0.f;
   }
-  __syncthreads();
+  // 64 x kSRows outputs of each product: 32 tiles, kTPW per warp, accumulated over the
+  // passes; <dS_C, S_0> over this block's key rows on the way
+  const int warp = tid >> 5;
+  const int m0 = ((warp * kTPW) >> 3) * 16, nb = ((warp * kTPW) & 7) * 8;
+  float aqs[kTPW][4] = {}, aks[kTPW][4] = {}, aws[kTPW][4] = {};
+  float part = 0.f;
+#pragma unroll 1
+  for (int c0 = 0; c0 < D; c0 += kSCols) {
+    if (c0 > 0) __syncthreads();  // the previous pass has read its tiles
+    tile_bf16_raw<kSRows, kSCols, kChunkThreads>(S0, LB, hc + c0, D, kSRows, true);
+    tile_f32<kSRows, kSCols, kChunkThreads>(dS, LF, dhc + c0, D, kSRows);
+    tile_bf16_raw<64, kSCols, kChunkThreads>(Dos, LB, bf_row(dout, t0, h) + c0, dout.st, len, vec);
+    tile_bf16_raw<64, kSCols, kChunkThreads>(Vp, LB, bf_row(v_new, t0, h) + c0, v_new.st, len, true);
+    tile_f32<64, kSCols, kChunkThreads>(dV, LF, dvt + c0, dvp.st, len);
+    __syncthreads();
+    mma_16xN<kTPW>(aqs, SMatH{Dos, LB, 1}, m0, SMatH{S0, 1, LB}, nb, 0, kSCols);
+    mma_16xN<kTPW>(aks, SMatH{Vp, LB, 1}, m0, SMat{dS, 1, LF}, nb, 0, kSCols);
+    mma_16xN<kTPW>(aws, SMat{dV, LF, 1}, m0, SMatH{S0, 1, LB}, nb, 0, kSCols);
+    for (int idx = tid; idx < kSRows * kSCols; idx += blockDim.x) {
+      const int r = idx / kSCols, j = idx % kSCols;
+      part += dS[r * LF + j] * __bfloat162float(S0[r * LB + j]);
+    }
+  }
   float *q_out = reinterpret_cast<float *>(dqh.p), *k_out = reinterpret_cast<float *>(dkh.p);
   float *w_out = reinterpret_cast<float *>(dw.p);
-  // 64 x kSRows outputs of each product: 32 tiles, four per warp
-  const int warp = tid >> 5;
-  {
-    const int m0 = ((warp * kTPW) >> 3) * 16, nb = ((warp * kTPW) & 7) * 8;
-    float aqs[kTPW][4] = {}, aks[kTPW][4] = {}, aws[kTPW][4] = {};
-    mma_16xN<kTPW>(aqs, SMat{Dos, L, 1}, m0, SMat{S0, 1, L}, nb, 0, D);
-    mma_16xN<kTPW>(aks, SMat{Vp, L, 1}, m0, SMat{dS, 1, L}, nb, 0, D);
-    mma_16xN<kTPW>(aws, SMat{dV, L, 1}, m0, SMat{S0, 1, L}, nb, 0, D);
 #pragma unroll
-    for (int b = 0; b < kTPW; ++b) {
-      const int n0 = nb + 8 * b;
-      float(&aq)[4] = aqs[b];
-      float(&ak)[4] = aks[b];
-      float(&aw)[4] = aws[b];
+  for (int b = 0; b < kTPW; ++b) {
+    const int n0 = nb + 8 * b;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = acc_row(m0, e), r = acc_col(n0, e);
-        if (i < len) {
-          q_out[(t0 + i) * dqh.st + h * dqh.sh + rb + r] = scale * EG[i] * aq[e];
-          k_out[(t0 + i) * dkh.st + h * dkh.sh + rb + r] = Dec[i] * ak[e];
-          w_out[(t0 + i) * dw.st + h * dw.sh + rb + r] = -aw[e];
-        }
+    for (int e = 0; e < 4; ++e) {
+      const int i = acc_row(m0, e), r = acc_col(n0, e);
+      if (i < len) {
+        q_out[(t0 + i) * dqh.st + h * dqh.sh + rb + r] = scale * EG[i] * aqs[b][e];
+        k_out[(t0 + i) * dkh.st + h * dkh.sh + rb + r] = Dec[i] * aks[b][e];
+        w_out[(t0 + i) * dw.st + h * dw.sh + rb + r] = -aws[b][e];
       }
     }
   }
-  // <dS_C, S_0> over this block's key rows (fixed-order tree reduction)
-  float part = 0.f;
-  for (int idx = tid; idx < kSRows * D; idx += blockDim.x) {
-    const int r = idx / D, j = idx % D;
-    part += dS[r * L + j] * S0[r * L + j];
-  }
+  // fixed-order tree reduction of the per-thread parts
   red[tid] = part;
   __syncthreads();
   for (int s = kChunkThreads / 2; s > 0; s >>= 1) {
@@ -758,8 +762,8 @@ cudaError_t launch_bwd_d(const BwdArgs &a, const BwdWs &w, cudaStream_t stream) 
   e = bcols == 64 ? scan(k_bwd_scan<D, 64>, 64, BwdScanSmem<D, 64>::bytes)
                   : scan(k_bwd_scan<D, 32>, 32, BwdScanSmem<D, 32>::bytes);
   if (e != cudaSuccess) return e;
-  if ((e = set_smem(k_bwd_sgrad<D>, SgradSmem<D>::bytes)) != cudaSuccess) return e;
-  k_bwd_sgrad<D><<<dim3(gc.x, gc.y, D / kSRows), kChunkThreads, SgradSmem<D>::bytes, stream>>>(
+  if ((e = set_smem(k_bwd_sgrad<D>, SgradSmem::bytes)) != cudaSuccess) return e;
+  k_bwd_sgrad<D><<<dim3(gc.x, gc.y, D / kSRows), kChunkThreads, SgradSmem::bytes, stream>>>(
       a.dout, vn, vg, a.scale, reinterpret_cast<const __nv_bfloat16 *>(w.h), w.dh, vdvp, vdqh,
       vdkh, vdw, w.sdot, a.chunks, a.n_chunks, s.H, vec);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
