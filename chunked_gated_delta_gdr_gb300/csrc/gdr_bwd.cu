@@ -28,8 +28,8 @@
 //
 // Kernels, in launch order (the forward recompute reuses the staged stage 1 and 2):
 //   k_bwd_dv_intra  dV' intra-chunk part                      (chunk, head, 64 columns)
-//   k_bwd_scan      dS_C per chunk, dV' total, dh0            (segment, head, 32 columns)
-//   k_bwd_sgrad     the S_0 / dS_C products: dQ, dK, dW parts (chunk, head, 32 key rows)
+//   k_bwd_scan      dS_C per chunk, dV' total, dh0            (segment, head, 32 or 64 columns)
+//   k_bwd_sgrad     the S_0 / dS_C products: dQ, dK, dW parts (chunk, head, 64 key rows)
 //   k_bwd_intra     E, the intra-chunk parts of dQ, dK, dG    (chunk, head)
 //   k_bwd_wy        the WY / solve backward, dv, dbeta, dg    (chunk, head)
 //   k_bwd_heads     per-value-head dq, dk summed over grouped heads, in head order
@@ -444,155 +444,178 @@ __global__ void __launch_bounds__(kChunkThreads, 2)
 }
 
 // ---------------------------------------------------------------- WY / solve backward
-template <int D>
+// The products that reduce over (or produce) the value dimension take it 64 columns at a
+// time, from tiles reloaded per pass (K, V bf16 as in memory; dV', dW fp32); the key
+// products K K^T stay in registers in the tile layout that dA has later, so the block
+// holds only the 64-column tiles and three 64 x 64 fp32 matrices: 111 KB, two blocks on
+// an SM.  The solve's scratch reuses the pass tiles.
+constexpr int kWyCols = 64;
 struct WySmem {
-  static constexpr int kLd = ld_rows(D), kLdK = ld_rows(64), kLdT = ld_cols(64);
-  static constexpr size_t bytes =
-      sizeof(float) * (4 * 64 * kLd + 64 * kLdK + 3 * 64 * kLdT + (5 + 4 * kQ) * 64 +
-                       kSolveScratch);
+  static constexpr int kLdB = ld_bf16(kWyCols), kLdF = ld_rows(kWyCols), kLdT = ld_cols(64);
+  static constexpr size_t pass_bytes =
+      sizeof(__nv_bfloat16) * 2 * 64 * kLdB + sizeof(float) * 2 * 64 * kLdF;
+  static constexpr size_t f32 = 3 * 64 * kLdT + 5 * 64 + 4 * kQ * 64;  // floats after the pass tiles
+  static constexpr size_t bytes = pass_bytes + sizeof(float) * f32;
+  static_assert(pass_bytes % 16 == 0 && pass_bytes >= sizeof(float) * kSolveScratch, "layout");
 };
 
 template <int D>
-__global__ void __launch_bounds__(kChunkThreads)
+__global__ void __launch_bounds__(kChunkThreads, 2)
     k_bwd_wy(int32_t group, View k, View v, View beta, View gcum, View dvp, View dw, View dkh,
              const float *dga, const float *sdot, View dv_out, View dbeta_out, View dg_out,
              const ChunkInfo *__restrict__ chunks, const int32_t *__restrict__ n_chunks,
              int32_t H, bool vec) {
   extern __shared__ float sm[];
-  constexpr int L = WySmem<D>::kLd, LK = WySmem<D>::kLdK, LT = WySmem<D>::kLdT;
+  constexpr int LB = WySmem::kLdB, LF = WySmem::kLdF, LT = WySmem::kLdT;
+  static_assert(kQ == 4 && kTPW == 2, "tile mapping below");
   const int cid = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   if (cid >= *n_chunks) return;
   const ChunkInfo ci = chunks[cid];
   const int len = ci.len, hk = h / group;
   const int64_t t0 = ci.start;
-  float *Ks = sm, *Vs = Ks + 64 * L, *dVs = Vs + 64 * L, *dWs = dVs + 64 * L;
-  float *KK = dWs + 64 * L, *Tm = KK + 64 * LK, *dT = Tm + 64 * LT, *X = dT + 64 * LT;
+  uint8_t *base = reinterpret_cast<uint8_t *>(sm);
+  __nv_bfloat16 *Ks = reinterpret_cast<__nv_bfloat16 *>(base), *Vs = Ks + 64 * LB;
+  float *dVs = reinterpret_cast<float *>(base + sizeof(__nv_bfloat16) * 2 * 64 * LB);
+  float *dWs = dVs + 64 * LF;
+  float *scratch = reinterpret_cast<float *>(base);  // during the solve only
+  float *Tm = reinterpret_cast<float *>(base + WySmem::pass_bytes), *dT = Tm + 64 * LT,
+        *X = dT + 64 * LT;
   float *G = X + 64 * LT, *B = G + 64, *BG = B + 64, *EGv = BG + 64, *dGt = EGv + 64;
-  float *baP = dGt + 64, *bbP = baP + kQ * 64;  // [kQ][64] partial row sums
-  float *scratch = bbP + kQ * 64;
-  const float *dvt = reinterpret_cast<const float *>(dvp.p), *dwt = reinterpret_cast<const float *>(dw.p);
-  tile_bf16<64, D, kChunkThreads>(Ks, L, bf_row(k, t0, hk), k.st, len, vec);
-  tile_bf16<64, D, kChunkThreads>(Vs, L, bf_row(v, t0, h), v.st, len, vec);
-  tile_f32<64, D, kChunkThreads>(dVs, L, dvt + t0 * dvp.st + h * dvp.sh, dvp.st, len);
-  tile_f32<64, D, kChunkThreads>(dWs, L, dwt + t0 * dw.st + h * dw.sh, dw.st, len);
+  float *baP = dGt + 64, *bbP = baP + kQ * 64;    // [kQ][64] partial row sums (dbeta)
+  float *rowP = bbP + kQ * 64, *colP = rowP + kQ * 64;  // [4][64] partial sums of P
+  const float *dvt = reinterpret_cast<const float *>(dvp.p) + t0 * dvp.st + h * dvp.sh;
+  const float *dwt = reinterpret_cast<const float *>(dw.p) + t0 * dw.st + h * dw.sh;
+  auto load_pass = [&](int c0) {
+    tile_bf16_raw<64, kWyCols, kChunkThreads>(Ks, LB, bf_row(k, t0, hk) + c0, k.st, len, vec);
+    tile_bf16_raw<64, kWyCols, kChunkThreads>(Vs, LB, bf_row(v, t0, h) + c0, v.st, len, vec);
+    tile_f32<64, kWyCols, kChunkThreads>(dVs, LF, dvt + c0, dvp.st, len);
+    tile_f32<64, kWyCols, kChunkThreads>(dWs, LF, dwt + c0, dw.st, len);
+  };
   if (tid < 64) {
     const bool in = tid < len;
-    G[tid] = in ? ldf(gcum.p, (t0 + tid) * gcum.st + h * gcum.sh) : 0.f;
-    B[tid] = in ? ldbf(beta.p, (t0 + tid) * beta.st + h * beta.sh) : 0.f;
+    const float gi = in ? ldf(gcum.p, (t0 + tid) * gcum.st + h * gcum.sh) : 0.f;
+    const float bi = in ? ldbf(beta.p, (t0 + tid) * beta.st + h * beta.sh) : 0.f;
+    const float ei = in ? expf(gi) : 0.f;
+    G[tid] = gi;
+    B[tid] = bi;
+    EGv[tid] = ei;
+    BG[tid] = bi * ei;
   }
   const int warp = tid >> 5;
-  // this thread's elements of the dK accumulator, loaded early (used at the end)
-  float *dvo = reinterpret_cast<float *>(dv_out.p), *dko = reinterpret_cast<float *>(dkh.p);
-  const int m0 = (warp & 3) * 16, cg = warp >> 2;
-  constexpr int kCT = D / (8 * kQ);
-  float kpre[kCT][4];
+  // 64 x 64 products: warp w owns tiles (m0, nb) and (m0, nb + 8)
+  const int tm0 = ((warp * kTPW) >> 3) * 16, tnb = ((warp * kTPW) & 7) * 8;
+  // raw key products k_i . k_j, dU_i . v_j and dW_i . k_j over the value passes
+  float kk[kTPW][4] = {}, du[kTPW][4] = {}, dwk[kTPW][4] = {};
+#pragma unroll 1
+  for (int c0 = 0; c0 < D; c0 += kWyCols) {
+    if (c0 > 0) __syncthreads();
+    load_pass(c0);
+    __syncthreads();
+    mma_16xN<kTPW>(kk, SMatH{Ks, LB, 1}, tm0, SMatH{Ks, 1, LB}, tnb, 0, kWyCols);
+    mma_16xN<kTPW>(du, SMat{dVs, LF, 1}, tm0, SMatH{Vs, 1, LB}, tnb, 0, kWyCols);
+    mma_16xN<kTPW>(dwk, SMat{dWs, LF, 1}, tm0, SMatH{Ks, 1, LB}, tnb, 0, kWyCols);
+  }
+  // A_ij = beta_i Gam_ij k_i . k_j into X (the solve's input) and dT_ij = beta_j (dU_i . v_j)
+  // + beta_j e^{G_j} (dW_i . k_j), i > j (the only part dA needs)
 #pragma unroll
-  for (int c = 0; c < kCT; ++c)
+  for (int b = 0; b < kTPW; ++b)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const int j = acc_row(m0, e), d = acc_col((cg * kCT + c) * 8, e);
-      kpre[c][e] = j < len ? dko[(t0 + j) * dkh.st + h * dkh.sh + d] : 0.f;
+      const int i = acc_row(tm0, e), j = acc_col(tnb + 8 * b, e);
+      const bool lo = j < i && i < len;
+      kk[b][e] = lo ? kk[b][e] : 0.f;
+      X[i * LT + j] = lo ? B[i] * expf(G[i] - G[j]) * kk[b][e] : 0.f;
+      dT[i * LT + j] = lo ? B[j] * du[b][e] + BG[j] * dwk[b][e] : 0.f;
     }
-  __syncthreads();
-  if (tid < 64) {
-    EGv[tid] = tid < len ? expf(G[tid]) : 0.f;
-    BG[tid] = B[tid] * EGv[tid];
-  }
-  // raw key products k_i . k_j (j < i) and A_ij = beta_i Gam_ij k_i . k_j
-  {
-    const int m0 = ((warp * kTPW) >> 3) * 16, nb = ((warp * kTPW) & 7) * 8;
-    float accs[kTPW][4] = {};
-    mma_16xN<kTPW>(accs, SMat{Ks, L, 1}, m0, SMat{Ks, 1, L}, nb, 0, D);
-#pragma unroll
-    for (int b = 0; b < kTPW; ++b) {
-      const int n0 = nb + 8 * b;
-      float(&acc)[4] = accs[b];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = acc_row(m0, e), j = acc_col(n0, e);
-        const bool lo = j < i && i < len;
-        KK[i * LK + j] = lo ? acc[e] : 0.f;
-        X[i * LT + j] = lo ? B[i] * expf(G[i] - G[j]) * acc[e] : 0.f;
-      }
-    }
-  }
-  __syncthreads();
-  constexpr int kSolveWarps = 4;
-  if (warp < kSolveWarps) {
-    // T = (I + A)^-1 on warps 0-3 (named barrier 1) ...
-    solve_unit_lower64(X, LT, Tm, LT, scratch, kSolveWarps * 32, 1);
-  } else {
-    // ... while the others form dT_ij = beta_j (dU_i . v_j) + beta_j e^{G_j} (dW_i . k_j),
-    // i > j (the only part dA needs), which does not need T
-    for (int tl = warp - kSolveWarps; tl < 32; tl += kWarps - kSolveWarps) {
-      const int m0 = (tl >> 3) * 16, n0 = (tl & 7) * 8;
-      float du[4] = {0.f, 0.f, 0.f, 0.f}, dwk[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_16x8(du, SMat{dVs, L, 1}, m0, SMat{Vs, 1, L}, n0, 0, D);
-      mma_16x8(dwk, SMat{dWs, L, 1}, m0, SMat{Ks, 1, L}, n0, 0, D);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = acc_row(m0, e), j = acc_col(n0, e);
-        dT[i * LT + j] = (j < i && i < len) ? B[j] * du[e] + BG[j] * dwk[e] : 0.f;
-      }
-    }
-  }
-  __syncthreads();
+  __syncthreads();  // also: every warp is done with the pass tiles (the solve's scratch)
+  solve_unit_lower64(X, LT, Tm, LT, scratch, kChunkThreads, 0);  // T = (I + A)^-1
   // X = dT T^T
   {
-    const int m0 = ((warp * kTPW) >> 3) * 16, nb = ((warp * kTPW) & 7) * 8;
     float accs[kTPW][4] = {};
-    mma_16xN<kTPW>(accs, SMat{dT, LT, 1}, m0, SMat{Tm, 1, LT}, nb, 0, 64);
+    mma_16xN<kTPW>(accs, SMat{dT, LT, 1}, tm0, SMat{Tm, 1, LT}, tnb, 0, 64);
 #pragma unroll
-    for (int b = 0; b < kTPW; ++b) {
-      const int n0 = nb + 8 * b;
-      float(&acc)[4] = accs[b];
+    for (int b = 0; b < kTPW; ++b)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) X[acc_row(m0, e) * LT + acc_col(n0, e)] = acc[e];
-    }
+      for (int e = 0; e < 4; ++e) X[acc_row(tm0, e) * LT + acc_col(tnb + 8 * b, e)] = accs[b][e];
   }
   __syncthreads();
-  // dA = -T^T X (i > j) into dT's place
+  // dA = -T^T X (i > j), in registers; P_ij = dA_ij Gam_ij (k_i . k_j) gives the dbeta term
+  // (row sums), and with B_ij = dA_ij beta_i Gam_ij the dG terms sum_j B_ij k_i.k_j =
+  // beta_i (row sum of P) and sum_i B_ij k_i.k_j (column sums of beta_i P_ij)
+  float dA[kTPW][4] = {};
+  mma_16xN<kTPW>(dA, SMat{Tm, 1, LT}, tm0, SMat{X, LT, 1}, tnb, 0, 64);
+  __syncthreads();  // every warp has read X
   {
-    const int m0 = ((warp * kTPW) >> 3) * 16, nb = ((warp * kTPW) & 7) * 8;
-    float accs[kTPW][4] = {};
-    mma_16xN<kTPW>(accs, SMat{Tm, 1, LT}, m0, SMat{X, LT, 1}, nb, 0, 64);
+    float rs[2] = {0.f, 0.f}, cs[kTPW][2] = {};
 #pragma unroll
-    for (int b = 0; b < kTPW; ++b) {
-      const int n0 = nb + 8 * b;
-      float(&acc)[4] = accs[b];
+    for (int b = 0; b < kTPW; ++b)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int i = acc_row(m0, e), j = acc_col(n0, e);
-        dT[i * LT + j] = (j < i && i < len) ? -acc[e] : 0.f;
+        const int i = acc_row(tm0, e), j = acc_col(tnb + 8 * b, e);
+        const bool lo = j < i && i < len;
+        const float gam = expf(G[i] - G[j]);
+        const float a = lo ? -dA[b][e] : 0.f;
+        const float pij = a * gam * kk[b][e];
+        X[i * LT + j] = a * B[i] * gam;
+        rs[e >> 1] += pij;
+        cs[b][e & 1] += B[i] * pij;
       }
+    // rows: the four lanes of a row (lane % 4); columns: the eight row groups (lane / 4)
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      rs[r] += __shfl_xor_sync(0xffffffffu, rs[r], 1);
+      rs[r] += __shfl_xor_sync(0xffffffffu, rs[r], 2);
+    }
+#pragma unroll
+    for (int b = 0; b < kTPW; ++b)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        cs[b][c] += __shfl_xor_sync(0xffffffffu, cs[b][c], 4);
+        cs[b][c] += __shfl_xor_sync(0xffffffffu, cs[b][c], 8);
+        cs[b][c] += __shfl_xor_sync(0xffffffffu, cs[b][c], 16);
+      }
+    const int lane = tid & 31;
+    if ((lane & 3) == 0) {
+      const int r0 = tm0 + (lane >> 2);
+      rowP[(warp & 3) * 64 + r0] = rs[0];
+      rowP[(warp & 3) * 64 + r0 + 8] = rs[1];
+    }
+    if (lane < 4) {
+#pragma unroll
+      for (int b = 0; b < kTPW; ++b)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) colP[(warp >> 2) * 64 + tnb + 8 * b + 2 * lane + c] = cs[b][c];
     }
   }
-  __syncthreads();
-  // X <- B_ij = dA_ij beta_i Gam_ij (i > j)
-  for (int idx = tid; idx < 64 * 64; idx += blockDim.x) {
-    const int i = idx / 64, j = idx % 64;
-    X[i * LT + j] = (j < i && i < len) ? dT[i * LT + j] * B[i] * expf(G[i] - G[j]) : 0.f;
-  }
-  __syncthreads();
-  // per row j: T^T dU, T^T dW, (B + B^T) K; warp w owns rows 16 (w % 4) .. +16 and column
-  // group w / 4
+  // per row j, for each value pass: T^T dU, T^T dW, (B + B^T) K; warp w owns rows
+  // 16 (w % 4) .. +16 and column group w / 4 of the pass
+  float *dvo = reinterpret_cast<float *>(dv_out.p), *dko = reinterpret_cast<float *>(dkh.p);
+  const int m0 = (warp & 3) * 16, cg = warp >> 2;
+  constexpr int kCT = kWyCols / (8 * kQ);
   float ba[2] = {0.f, 0.f}, bb[2] = {0.f, 0.f};
+#pragma unroll 1
+  for (int c0 = 0; c0 < D; c0 += kWyCols) {
+    __syncthreads();  // X written (first pass) / the previous pass's tiles read
+    load_pass(c0);
+    __syncthreads();
 #pragma unroll
-  for (int c = 0; c < kCT; ++c) {
-    const int n0 = (cg * kCT + c) * 8;
-    float tdu[4] = {0.f, 0.f, 0.f, 0.f}, tdw[4] = {0.f, 0.f, 0.f, 0.f}, kc[4] = {0.f, 0.f, 0.f, 0.f};
-    mma_16x8(tdu, SMat{Tm, 1, LT}, m0, SMat{dVs, L, 1}, n0, 0, 64);
-    mma_16x8(tdw, SMat{Tm, 1, LT}, m0, SMat{dWs, L, 1}, n0, 0, 64);
-    mma_16x8(kc, SMat{X, LT, 1}, m0, SMat{Ks, L, 1}, n0, 0, 64);
-    mma_16x8(kc, SMat{X, 1, LT}, m0, SMat{Ks, L, 1}, n0, 0, 64);
+    for (int c = 0; c < kCT; ++c) {
+      const int n0 = (cg * kCT + c) * 8;
+      float tdu[4] = {0.f, 0.f, 0.f, 0.f}, tdw[4] = {0.f, 0.f, 0.f, 0.f}, kc[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_16x8(tdu, SMat{Tm, 1, LT}, m0, SMat{dVs, LF, 1}, n0, 0, 64);
+      mma_16x8(tdw, SMat{Tm, 1, LT}, m0, SMat{dWs, LF, 1}, n0, 0, 64);
+      mma_16x8(kc, SMat{X, LT, 1}, m0, SMatH{Ks, LB, 1}, n0, 0, 64);
+      mma_16x8(kc, SMat{X, 1, LT}, m0, SMatH{Ks, LB, 1}, n0, 0, 64);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int j = acc_row(m0, e), d = acc_col(n0, e);
-      if (j < len) {
-        dvo[(t0 + j) * dv_out.st + h * dv_out.sh + d] = B[j] * tdu[e];
-        ba[e >> 1] += Vs[j * L + d] * tdu[e];
-        bb[e >> 1] += Ks[j * L + d] * tdw[e];
-        dko[(t0 + j) * dkh.st + h * dkh.sh + d] = kpre[c][e] + BG[j] * tdw[e] + kc[e];
+      for (int e = 0; e < 4; ++e) {
+        const int j = acc_row(m0, e), d = acc_col(n0, e);
+        if (j < len) {
+          const int64_t ok = (t0 + j) * dkh.st + h * dkh.sh + c0 + d;
+          dvo[(t0 + j) * dv_out.st + h * dv_out.sh + c0 + d] = B[j] * tdu[e];
+          ba[e >> 1] += __bfloat162float(Vs[j * LB + d]) * tdu[e];
+          bb[e >> 1] += __bfloat162float(Ks[j * LB + d]) * tdw[e];
+          dko[ok] = dko[ok] + BG[j] * tdw[e] + kc[e];
+        }
       }
     }
   }
@@ -611,40 +634,26 @@ __global__ void __launch_bounds__(kChunkThreads)
     bbP[cg * 64 + r0 + 8] = bb[1];
   }
   __syncthreads();
-  {
-    // row r = tid / 8; its 8 threads (neighbouring lanes) take every 8th index, then
-    // three shuffles add the parts in a fixed order
-    const int r = tid >> 3, part = tid & 7;
-    float dbc = 0.f, rowq = 0.f, colq = 0.f;
-    if (r < len) {
-      for (int x = part; x < r; x += 8) {
-        dbc += dT[r * LT + x] * expf(G[r] - G[x]) * KK[r * LK + x];
-        rowq += X[r * LT + x] * KK[r * LK + x];
-      }
-      for (int a = r + 1 + part; a < len; a += 8) colq += X[a * LT + r] * KK[a * LK + r];
+  if (tid < len) {
+    const int r = tid;
+    float dba = 0.f, dbb = 0.f, dbc = 0.f, colq = 0.f;
+    for (int q = 0; q < kQ; ++q) {
+      dba += baP[q * 64 + r];
+      dbb += bbP[q * 64 + r];
     }
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
-      dbc += __shfl_xor_sync(0xffffffffu, dbc, o);
-      rowq += __shfl_xor_sync(0xffffffffu, rowq, o);
-      colq += __shfl_xor_sync(0xffffffffu, colq, o);
+    for (int q = 0; q < 4; ++q) {
+      dbc += rowP[q * 64 + r];
+      colq += colP[q * 64 + r];
     }
-    if (r < len && part == 0) {
-      float dba = 0.f, dbb = 0.f;
-      for (int q = 0; q < kQ; ++q) {
-        dba += baP[q * 64 + r];
-        dbb += bbP[q * 64 + r];
-      }
-      float *dbo = reinterpret_cast<float *>(dbeta_out.p);
-      dbo[(t0 + r) * dbeta_out.st + h * dbeta_out.sh] = dba + EGv[r] * dbb + dbc;
-      float gt = dga[(t0 + r) * H + h] + BG[r] * dbb + rowq - colq;
-      if (r == len - 1) {
-        float sd = 0.f;
-        for (int b = 0; b < D / kSRows; ++b) sd += sdot[((int64_t)cid * H + h) * (D / kSRows) + b];
-        gt += EGv[r] * sd;
-      }
-      dGt[r] = gt;
+    float *dbo = reinterpret_cast<float *>(dbeta_out.p);
+    dbo[(t0 + r) * dbeta_out.st + h * dbeta_out.sh] = dba + EGv[r] * dbb + dbc;
+    float gt = dga[(t0 + r) * H + h] + BG[r] * dbb + B[r] * dbc - colq;
+    if (r == len - 1) {
+      float sd = 0.f;
+      for (int b = 0; b < D / kSRows; ++b) sd += sdot[((int64_t)cid * H + h) * (D / kSRows) + b];
+      gt += EGv[r] * sd;
     }
+    dGt[r] = gt;
   }
   __syncthreads();
   if (tid < len) {  // dg = reverse cumulative sum of dG inside the chunk
@@ -772,8 +781,8 @@ cudaError_t launch_bwd_d(const BwdArgs &a, const BwdWs &w, cudaStream_t stream) 
                                                             a.scale, vdqh, vdkh, w.dga,
                                                             a.chunks, a.n_chunks, s.H, vec);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if ((e = set_smem(k_bwd_wy<D>, WySmem<D>::bytes)) != cudaSuccess) return e;
-  k_bwd_wy<D><<<gc, kChunkThreads, WySmem<D>::bytes, stream>>>(group, a.k, a.v, a.beta, vg, vdvp, vdw,
+  if ((e = set_smem(k_bwd_wy<D>, WySmem::bytes)) != cudaSuccess) return e;
+  k_bwd_wy<D><<<gc, kChunkThreads, WySmem::bytes, stream>>>(group, a.k, a.v, a.beta, vg, vdvp, vdw,
                                                       vdkh, w.dga, w.sdot, a.dv, a.dbeta, a.dg,
                                                       a.chunks, a.n_chunks, s.H, vec);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
