@@ -1,6 +1,7 @@
 // gdr_bwd.cu -- backward of the chunked gated delta rule: dq, dk, dv, dg, dbeta, dh0 from
-// dL/do and dL/dht.  fp32 shared-memory tiles; the dense products run on the tensor
-// pipe as warp tiles (tf32 in, fp32 accumulate, gdr_mma.cuh), the rest in fp32 SIMT.
+// dL/do and dL/dht.  Shared-memory operand tiles in bf16 where their values are bf16
+// (inputs and the bf16 intermediates) and fp32 otherwise; the dense products run on the
+// tensor pipe as warp tiles (tf32 in, fp32 accumulate, gdr_mma.cuh), the rest in fp32 SIMT.
 //
 // The pages describe a training backend whose backward is bit-reproducible and
 // tolerates length-0 segments ("Findings from integrating FlashQLA's Blackwell GDN

@@ -1,6 +1,6 @@
 // gdr_mma.cuh -- for the staged and backward kernels: warp-level tensor-core tiles over
-// fp32 shared-memory operands (tf32 in, fp32 accumulate, mma.sync m16n8k8), and tile
-// loads from global memory into fp32 shared memory.
+// fp32 or bf16 shared-memory operands (tf32 in, fp32 accumulate, mma.sync m16n8k8), and
+// tile loads from global memory into shared memory.
 #pragma once
 
 #include <cuda_bf16.h>

@@ -1,8 +1,8 @@
 // gdr_staged.cu -- the three stages of the chunked gated delta rule forward as
 // separate kernels with their intermediates in HBM (GDR_PATH_STAGED and the
-// per-stage entry points).  fp32 arithmetic over shared-memory tiles (the state
-// scan's products as tf32 tensor-core warp tiles, the rest SIMT); bf16 at the same
-// storage points as the fused path (W, U, V', h).
+// per-stage entry points).  fp32 arithmetic; every dense product as tf32 tensor-core
+// warp tiles over shared-memory operands (bf16 tiles for bf16 values, fp32 otherwise),
+// the rest SIMT; bf16 at the same storage points as the fused path (W, U, V', h).
 //
 // Per chunk of 64 tokens (chunk-local indices i, j) and value head:
 //   stage 1  G = cumsum(g);  A_ij = beta_i e^{G_i-G_j} k_i.k_j (j<i);  Tm = (I+A)^-1
