@@ -542,7 +542,9 @@ __global__ void __launch_bounds__(kChunkThreads, 2)
   __syncthreads();
   // dA = -T^T X (i > j), in registers; P_ij = dA_ij Gam_ij (k_i . k_j) gives the dbeta term
   // (row sums), and with B_ij = dA_ij beta_i Gam_ij the dG terms sum_j B_ij k_i.k_j =
-  // beta_i (row sum of P) and sum_i B_ij k_i.k_j (column sums of beta_i P_ij)
+  // beta_i (row sum of P) and sum_i B_ij k_i.k_j (column sums of beta_i P_ij).  X then
+  // holds B + B^T (B is strictly lower: the owner of (i, j), i > j, writes both halves,
+  // the diagonal is zero), which is symmetric, so (B + B^T) K is one product.
   float dA[kTPW][4] = {};
   mma_16xN<kTPW>(dA, SMat{Tm, 1, LT}, tm0, SMat{X, LT, 1}, tnb, 0, 64);
   __syncthreads();  // every warp has read X
@@ -557,7 +559,13 @@ __global__ void __launch_bounds__(kChunkThreads, 2)
         const float gam = expf(G[i] - G[j]);
         const float a = lo ? -dA[b][e] : 0.f;
         const float pij = a * gam * kk[b][e];
-        X[i * LT + j] = a * B[i] * gam;
+        if (j < i) {
+          const float bij = a * B[i] * gam;
+          X[i * LT + j] = bij;
+          X[j * LT + i] = bij;
+        } else if (j == i) {
+          X[i * LT + j] = 0.f;
+        }
         rs[e >> 1] += pij;
         cs[b][e & 1] += B[i] * pij;
       }
@@ -605,8 +613,7 @@ __global__ void __launch_bounds__(kChunkThreads, 2)
       float tdu[4] = {0.f, 0.f, 0.f, 0.f}, tdw[4] = {0.f, 0.f, 0.f, 0.f}, kc[4] = {0.f, 0.f, 0.f, 0.f};
       mma_16x8(tdu, SMat{Tm, 1, LT}, m0, SMat{dVs, LF, 1}, n0, 0, 64);
       mma_16x8(tdw, SMat{Tm, 1, LT}, m0, SMat{dWs, LF, 1}, n0, 0, 64);
-      mma_16x8(kc, SMat{X, LT, 1}, m0, SMatH{Ks, LB, 1}, n0, 0, 64);
-      mma_16x8(kc, SMat{X, 1, LT}, m0, SMatH{Ks, LB, 1}, n0, 0, 64);
+      mma_16x8(kc, SMat{X, 1, LT}, m0, SMatH{Ks, LB, 1}, n0, 0, 64);  // (B + B^T) K
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int j = acc_row(m0, e), d = acc_col(n0, e);
