@@ -229,12 +229,12 @@ __global__ void __launch_bounds__(kScanCols * 4)
 constexpr int kSRows = 64;  // key rows of S_0 / dS_C per block
 
 // The products reduce over the value dimension, taken 64 columns at a time: per pass
-// S_0, dO, V' as bf16 (their values are bf16) and dS_C, dV' as fp32, 65 KB, so two
+// S_0, dO, V' as bf16 (their values are bf16) and dS_C, dV' as fp32, 63 KB, so two
 // blocks fit on an SM.
 constexpr int kSCols = 64;
 struct SgradSmem {
   static constexpr int kLdB = ld_bf16(kSCols), kLdF = ld_rows(kSCols);
-  static constexpr size_t f32 = (kSRows + 64) * kLdF + 2 * 64 + kChunkThreads;  // floats
+  static constexpr size_t f32 = (kSRows + 64) * kLdF + 2 * 64 + kWarps;  // floats
   static constexpr size_t bytes =
       sizeof(float) * f32 + sizeof(__nv_bfloat16) * (kSRows + 2 * 64) * kLdB;
 };
@@ -302,14 +302,17 @@ __global__ void __launch_bounds__(kChunkThreads, 2)
       }
     }
   }
-  // fixed-order tree reduction of the per-thread parts
-  red[tid] = part;
+  // the per-thread parts summed in a fixed order: a shuffle tree in each warp, then the
+  // warps' sums in warp order
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  if ((tid & 31) == 0) red[warp] = part;
   __syncthreads();
-  for (int s = kChunkThreads / 2; s > 0; s >>= 1) {
-    if (tid < s) red[tid] += red[tid + s];
-    __syncthreads();
+  if (tid == 0) {
+    float t = 0.f;
+    for (int w = 0; w < kWarps; ++w) t += red[w];
+    sdot[((int64_t)cid * H + h) * (D / kSRows) + blockIdx.z] = t;
   }
-  if (tid == 0) sdot[((int64_t)cid * H + h) * (D / kSRows) + blockIdx.z] = red[0];
 }
 
 // ---------------------------------------------------------------- intra-chunk terms
@@ -605,6 +608,16 @@ __global__ void __launch_bounds__(kChunkThreads, 2)
 #pragma unroll 1
   for (int c0 = 0; c0 < D; c0 += kWyCols) {
     __syncthreads();  // X written (first pass) / the previous pass's tiles read
+    // this thread's dK accumulator elements (written by earlier kernels), loaded with the
+    // pass's tiles so that the loads overlap
+    float kpre[kCT][4];
+#pragma unroll
+    for (int c = 0; c < kCT; ++c)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = acc_row(m0, e), d = acc_col((cg * kCT + c) * 8, e);
+        kpre[c][e] = j < len ? dko[(t0 + j) * dkh.st + h * dkh.sh + c0 + d] : 0.f;
+      }
     load_pass(c0);
     __syncthreads();
 #pragma unroll
@@ -618,11 +631,10 @@ __global__ void __launch_bounds__(kChunkThreads, 2)
       for (int e = 0; e < 4; ++e) {
         const int j = acc_row(m0, e), d = acc_col(n0, e);
         if (j < len) {
-          const int64_t ok = (t0 + j) * dkh.st + h * dkh.sh + c0 + d;
           dvo[(t0 + j) * dv_out.st + h * dv_out.sh + c0 + d] = B[j] * tdu[e];
           ba[e >> 1] += __bfloat162float(Vs[j * LB + d]) * tdu[e];
           bb[e >> 1] += __bfloat162float(Ks[j * LB + d]) * tdw[e];
-          dko[ok] = dko[ok] + BG[j] * tdw[e] + kc[e];
+          dko[(t0 + j) * dkh.st + h * dkh.sh + c0 + d] = kpre[c][e] + BG[j] * tdw[e] + kc[e];
         }
       }
     }
