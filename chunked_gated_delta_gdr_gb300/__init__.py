@@ -20,6 +20,7 @@ from .api import (  # noqa: F401
     clear_device_status,
     device_status,
     split_pieces,
+    split_plan,
     stage_workspace_bytes,
     state_scan,
     wait_selftest,

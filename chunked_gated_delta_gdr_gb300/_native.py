@@ -42,6 +42,7 @@ SIGNATURES = {
     "gdr_chunk_bwd_workspace_bytes": (_sz, [_i64, _i32, _i32, _i32, _i32, _i32]),
     "gdr_ckpt_count_bound": (_i64, [_i64, _i32]),
     "gdr_fused_split_pieces": (_i32, [_i64, _i32, _i32]),
+    "gdr_split_plan": (_i32, [_i64, _i32, _vp]),
     "gdr_chunk_count_bound": (_i64, [_i64, _i32]),
     "gdr_stage_workspace_bytes": (_sz, [_i64, _i32]),
     "gdr_chunk_index": (ctypes.c_int, [_vp, _i32, _i64, _vp, _vp, _vp, _vp]),

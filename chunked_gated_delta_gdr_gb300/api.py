@@ -434,6 +434,14 @@ def split_pieces(T: int, n_seq: int, H: int) -> int:
     return int(nat.lib().gdr_fused_split_pieces(T, n_seq, H))
 
 
+def split_plan(units: int, sms: int) -> tuple:
+    """The split planner for ``units`` (segment, value head) pairs on ``sms`` SMs:
+    (pieces per long segment, first piece's weight); (1, 1) means no split."""
+    lead = ctypes.c_int32(1)
+    pieces = int(nat.lib().gdr_split_plan(units, sms, ctypes.byref(lead)))
+    return pieces, int(lead.value)
+
+
 def checkpoint_count_bound(T: int, checkpoint_every_n_tokens: int) -> int:
     """Rows ``chunk_fwd_checkpoints`` may write: floor(T / checkpoint_every_n_tokens)."""
     return int(nat.lib().gdr_ckpt_count_bound(T, checkpoint_every_n_tokens))

@@ -371,6 +371,13 @@ int32_t gdr_fused_split_pieces(int64_t T, int32_t n_seq, int32_t H) {
   return split_plan(T, n_seq, H, false);
 }
 
+int32_t gdr_split_plan(int64_t units, int32_t sms, int32_t *lead) {
+  int l = 1;
+  const int p = split_pieces(units, sms, &l);
+  if (lead) *lead = l;
+  return p;
+}
+
 int64_t gdr_ckpt_count_bound(int64_t T, int32_t ckpt_every) {
   if (T < 0 || ckpt_every <= 0) return 0;
   return T / ckpt_every;

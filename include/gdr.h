@@ -174,6 +174,17 @@ int64_t gdr_ckpt_count_bound(int64_t T, int32_t checkpoint_every_n_tokens);
  * queried. */
 int32_t gdr_fused_split_pieces(int64_t T, int32_t n_seq, int32_t H);
 
+/* The split planner behind gdr_fused_split_pieces, for any machine size: for `units`
+ * (segment, value head) pairs on `sms` SMs, the pieces per long segment (1: no split;
+ * else 3..8) and, in *lead (may be NULL), the first piece's weight (1..3).  The plan
+ * minimises pass A + pass B of the split in units of the whole segment: pass A runs the
+ * first pieces (weight `lead`) and, for every middle piece, its state map's offset R and
+ * transition M (weight 1 each); pass B the P - 1 later pieces; each pass on `sms` SMs
+ * taking units in that order as they come free; ties go to fewer pieces, and no split
+ * unless 3 * units <= sms.  Pure host arithmetic; non-positive arguments give 1 and
+ * lead 1. */
+int32_t gdr_split_plan(int64_t units, int32_t sms, int32_t *lead);
+
 /*
  * gdr_chunk_bwd -- the backward: gradients of gdr_chunk_fwd's outputs with respect to
  * all its inputs.  FlashQLA's GDN kernels serve as a training backend whose backward
