@@ -559,7 +559,9 @@ __global__ void __launch_bounds__(kChunkThreads, 2)
       for (int e = 0; e < 4; ++e) {
         const int i = acc_row(tm0, e), j = acc_col(tnb + 8 * b, e);
         const bool lo = j < i && i < len;
-        const float gam = expf(G[i] - G[j]);
+        // the decay only where it is a ratio e^{G_i - G_j}, j < i (at most 1 for g <= 0):
+        // elsewhere e^{G_i - G_j} can overflow and 0 * inf would be NaN
+        const float gam = lo ? expf(G[i] - G[j]) : 0.f;
         const float a = lo ? -dA[b][e] : 0.f;
         const float pij = a * gam * kk[b][e];
         if (j < i) {

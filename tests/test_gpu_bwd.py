@@ -244,3 +244,20 @@ def test_pipelined_host_backward_matches_device(parts):
         else:
             assert torch.equal(a[:w.T], b.cpu()), name
             assert not a[w.T:].any(), name
+
+
+def test_backward_strong_decays_stay_finite():
+    """Decays of about e^-6 per token: within a chunk the cumulative gate spans several
+    hundred, so e^{G_i - G_j} is only finite as a ratio with j < i, and a partial chunk's
+    padded rows sit far above its real ones.  Every gradient must stay finite and match
+    the oracle."""
+    w = make_workload("strong_decay", 97, [150, 37, 64], 1, 2, 64, with_h0=True)
+    gen = torch.Generator().manual_seed(98)
+    w.g = -6.0 + 0.5 * torch.randn(w.T, w.H, generator=gen)
+    do, dht = _upstream(w, 99, True)
+    ref = oracle.recurrent_bwd(w.q, w.k, w.v, w.g, w.beta, w.scale, w.h0, w.cu_seqlens, do, dht)
+    got = _run_bwd(w, do, dht)
+    mask = covered_tokens(w.cu_seqlens, w.T)
+    for name, a, b in zip(NAMES, got, ref):
+        assert torch.isfinite(a).all(), name
+        _close(name, a, b, None if name == "dh0" else mask)
