@@ -11,7 +11,8 @@ section 2) but print no backward formula.  Sources of truth used here:
   * splitting a segment and chaining its gradients through dht -> dh0 (the backward
     of the ht -> h0 chaining invariant);
   * length-0 segments: they change no gradient, and their dh0 is their dht;
-  * the beta = 0 closed form (pure decay: S_t = e^{G_t} h0).
+  * the beta = 0 closed form (pure decay: S_t = e^{G_t} h0);
+  * the strong-decay limit (g = -60: every token starts from a wiped state).
 
 Every pin takes the forward and backward as callables, so the same pins also run
 against deliberately broken copies of the backward (mutation tests at the bottom).
@@ -150,8 +151,40 @@ def pin_bwd_beta_zero(fwd, bwd):
     np.testing.assert_allclose(gr["h0"][0, 0], dh0, rtol=0, atol=1e-12)
 
 
+def pin_bwd_strong_decay(fwd, bwd):
+    # g = -60: alpha = e^-60 ~ 1e-26 wipes the previous state at every token, so
+    # S_t = beta_t k_t v_t^T up to terms ~1e-26, o_t = scale beta_t (q_t . k_t) v_t, and
+    # with L = sum_t <o_t, do_t> + <ht, dht> (ht = S_last):
+    #   dq_t = scale beta_t (v_t . do_t) k_t
+    #   dk_t = scale beta_t (v_t . do_t) q_t      (+ beta dht v at the last token)
+    #   dv_t = scale beta_t (q_t . k_t) do_t      (+ beta dht^T k at the last token)
+    #   dbeta_t = scale (q_t . k_t)(v_t . do_t)   (+ k^T dht v at the last token)
+    #   dg, dh0 ~ 0
+    d = _problem(61, [9], 1, 1, 3, 2)
+    d["g"] = np.full_like(d["g"], -60.0)
+    o, ht = fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], d["h0"], d["cu"])
+    gr = _grads(bwd, d)
+    q, k, v, b, do, s = (d["q"][:, 0], d["k"][:, 0], d["v"][:, 0], d["beta"][:, 0],
+                         d["dout"][:, 0], d["scale"])
+    qk, vdo = (q * k).sum(1), (v * do).sum(1)
+    dht = d["dht"][0, 0]
+    np.testing.assert_allclose(o[:, 0], s * (b * qk)[:, None] * v, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(ht[0, 0], b[-1] * np.outer(k[-1], v[-1]), rtol=0, atol=1e-12)
+    dk = s * (b * vdo)[:, None] * q
+    dk[-1] += b[-1] * dht @ v[-1]
+    dv = s * (b * qk)[:, None] * do
+    dv[-1] += b[-1] * dht.T @ k[-1]
+    db = s * qk * vdo
+    db[-1] += k[-1] @ dht @ v[-1]
+    np.testing.assert_allclose(gr["q"][:, 0], s * (b * vdo)[:, None] * k, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(gr["k"][:, 0], dk, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(gr["v"][:, 0], dv, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(gr["beta"][:, 0], db, rtol=0, atol=1e-12)
+    assert np.abs(gr["g"]).max() < 1e-12 and np.abs(gr["h0"]).max() < 1e-12
+
+
 PINS = [pin_bwd_directional_fd, pin_bwd_elementwise_fd, pin_bwd_chaining, pin_bwd_ghosts,
-        pin_bwd_beta_zero]
+        pin_bwd_beta_zero, pin_bwd_strong_decay]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
