@@ -269,3 +269,12 @@ def test_backward_workspace_bytes(lib):
     assert lib.gdr_chunk_bwd_workspace_bytes(-1, N, Hk, H, D, D) == 0
     # one value head per key head needs no per-value-head scratch
     assert lib.gdr_chunk_bwd_workspace_bytes(T, N, H, H, D, D) < b
+
+
+def test_split_plan_entry_point(lib):
+    lead = ctypes.c_int32(0)
+    assert lib.gdr_split_plan(32, 152, ctypes.byref(lead)) == 5 and lead.value == 2
+    assert lib.gdr_split_plan(32, 152, None) == 5  # lead may be NULL
+    lead.value = 7
+    assert lib.gdr_split_plan(0, 152, ctypes.byref(lead)) == 1 and lead.value == 1
+    assert lib.gdr_split_plan(10, -1, None) == 1
