@@ -27,7 +27,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "GDR chunk-fwd tokens/s (H=32, d=128, 64k packed) & % of tensor/HBM roofline"
 WORKLOAD = "packed_64k_h32"
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gdr_fused_fwd_packed_64k_h32.md")
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "k_fused_traffic.json")
 
 
 def parse():
@@ -44,6 +44,13 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU seconds for the oracle sample")
+    p.add_argument("--record-traffic", metavar="NCU_CSV",
+                   help="write the fused kernel's traffic record from an ncu CSV log of "
+                        "dram__bytes_read.sum / dram__bytes_write.sum, then exit")
+    p.add_argument("--traffic-out", default=None,
+                   help="where --record-traffic writes (default: the committed record)")
+    p.add_argument("--traffic-command", default="",
+                   help="the capture command, stored in the record")
     return p.parse_args()
 
 
@@ -77,25 +84,6 @@ def algorithmic_flops(w) -> int:
     return int(f * w.H)
 
 
-def read_traffic(expected_sha: str):
-    """dram bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source (same sha256), else None."""
-    try:
-        txt = open(PROFILE_SUMMARY).read()
-    except OSError:
-        return None
-    sha = traffic = None
-    for line in txt.splitlines():
-        if line.startswith("source_sha256:"):
-            sha = line.split(":", 1)[1].strip()
-        if line.startswith("dram_bytes_per_launch:"):
-            try:
-                traffic = float(line.split(":", 1)[1].strip())
-            except ValueError:
-                traffic = None
-    return traffic if (sha and sha == expected_sha) else None
-
-
 # the sources the fused forward kernel is compiled from
 KERNEL_SOURCES = ("gdr_fused.cu", "gdr_internal.cuh", "gdr_tc.cuh")
 
@@ -107,6 +95,62 @@ def kernel_sha() -> str:
     for f in KERNEL_SOURCES:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
+
+
+def read_traffic(expected_sha: str, workload: str):
+    """DRAM bytes per launch of the fused kernel from the machine-written record of an
+    ncu capture (``--record-traffic``), scaled to ``workload``; None unless the record
+    was taken on the current kernel sources (same sha256) and names this workload."""
+    try:
+        rec = json.load(open(TRAFFIC_RECORD))
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_sha256") != expected_sha:
+        return None
+    scaled = rec.get("scaled", {}).get(workload)
+    return None if scaled is None else float(scaled["dram_bytes_per_launch"])
+
+
+def record_traffic(csv_path: str, case: str, out_path: str, command: str) -> int:
+    """Write the traffic record from an ncu CSV log of dram__bytes_read.sum and
+    dram__bytes_write.sum for k_fused launches of workload ``case``: bytes per launch
+    (mean over the captured launches), the sha256 of the kernel sources computed here,
+    and the figure scaled to the bench workload by algorithmic bytes (every token is
+    streamed once, so traffic grows in proportion to the tokens processed)."""
+    import csv
+    from chunked_gated_delta_gdr_gb300.inputs import make_named
+    launches = {}
+    with open(csv_path) as f:
+        rows = [ln for ln in f if ln.startswith('"')]
+    for row in csv.DictReader(rows):
+        if "k_fused" not in row["Kernel Name"]:
+            continue
+        m = row["Metric Name"]
+        if m in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            val = float(row["Metric Value"].replace(",", ""))
+            unit = row["Metric Unit"].lower()
+            val *= {"byte": 1, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9}.get(unit, 1)
+            launches.setdefault(row["ID"], {})[m] = val
+    full = [v for v in launches.values() if len(v) == 2]
+    if not full:
+        print(f"no k_fused dram counters in {csv_path}", file=sys.stderr)
+        return 1
+    rd = sum(v["dram__bytes_read.sum"] for v in full) / len(full)
+    wr = sum(v["dram__bytes_write.sum"] for v in full) / len(full)
+    wc = make_named(case)
+    alg_case = algorithmic_bytes(wc)
+    rec = {"kernel": "k_fused", "source_sha256": kernel_sha(), "case": case,
+           "launches": len(full), "dram_bytes_read": rd, "dram_bytes_write": wr,
+           "dram_bytes_per_launch": rd + wr, "algorithmic_bytes": alg_case,
+           "ratio_to_algorithmic": (rd + wr) / alg_case, "command": command, "scaled": {}}
+    for name in (case, WORKLOAD):
+        f = algorithmic_bytes(make_named(name)) / alg_case
+        rec["scaled"][name] = {"factor": f, "dram_bytes_per_launch": (rd + wr) * f}
+    with open(out_path, "w") as f:
+        json.dump(rec, f, indent=1)
+        f.write("\n")
+    print(json.dumps(rec))
+    return 0
 
 
 class ClockSampler:
@@ -330,7 +374,7 @@ def bench_ours(args):
                        "per_rank": "each rank runs its own copy of the workload"},
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
                          "frac": achieved_gbs / hbm, "peak_kind": f"{peak_kind} burst copy",
-                         "traffic": read_traffic(kernel_sha()),
+                         "traffic": read_traffic(kernel_sha(), w.name),
                          "algorithmic_bytes_per_launch": alg_b,
                          "tensor": {"achieved": achieved_tfs, "peak": tflops,
                                     "unit": "TFLOP/s", "frac": achieved_tfs / tflops,
@@ -603,6 +647,9 @@ def bench_reference_bwd(args):
 
 def main():
     args = parse()
+    if args.record_traffic:
+        return record_traffic(args.record_traffic, args.workload,
+                              args.traffic_out or TRAFFIC_RECORD, args.traffic_command)
     if args.op == "bwd":
         return bench_reference_bwd(args) if args.impl == "reference" else bench_ours_bwd(args)
     if args.impl == "reference":

@@ -34,7 +34,9 @@ def nvcc() -> str:
 
 
 def _deps():
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    """The compiled sources and every header they may include."""
+    files = [os.path.join(CSRC, f) for f in SOURCES]
+    files += [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     files.append(os.path.join(INCLUDE, "gdr.h"))
     files.append(os.path.abspath(__file__))
     return files

@@ -320,8 +320,10 @@ int gdr_debug_wait_selftest(uint32_t limit_us, cudaStream_t stream);
  * Scratch: the chunk tables (segment table, chunk table, chunk count) live in one static
  * device array of GDR_NOALLOC_SCRATCH_BYTES (4 MiB) inside libgdr; every GPU that loads
  * the library holds that array until the process exits.  A problem needs
- * 256 + 16 * max(n_seq, 1) + 16 * gdr_chunk_count_bound(T, n_seq) bytes, each term rounded
- * up to 256; larger problems return GDR_ERR_SCRATCH_LIMIT (roughly 260k chunks).
+ * 256 + 16 * max(n_seq, 1) + 16 * gdr_chunk_count_bound(T, n_seq) + 4 * max(n_seq, 1)
+ * bytes, each term rounded up to 256 (the chunk count, the segment table, the chunk
+ * table and the segment order); larger problems return GDR_ERR_SCRATCH_LIMIT (roughly
+ * 260k chunks).
  * The tables are rewritten completely by every call, so nothing needs clearing between
  * calls.  Every call on a device shares the same array: calls whose work overlaps on the
  * GPU (different streams without ordering between them) race and may produce wrong

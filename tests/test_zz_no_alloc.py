@@ -12,7 +12,7 @@ import torch
 from chunked_gated_delta_gdr_gb300 import _native as nat
 from chunked_gated_delta_gdr_gb300 import api
 from chunked_gated_delta_gdr_gb300.inputs import make_workload
-from gdr_testlib import O_ATOL, O_COS
+from gdr_testlib import O_ATOL, O_COS, assert_o_close, covered_tokens, oracle_heads
 
 pytestmark = pytest.mark.gpu
 
@@ -49,6 +49,10 @@ def test_noalloc_matches_workspace_entry_point_twice():
         got = api.chunk_out_noalloc(wd.q, wd.k, vn, h, gc, w.scale, wd.cu_seqlens)
         torch.cuda.synchronize()
         _close(got, ref)
+        # and directly against the fp64 token recurrence, so that a fault shared by both
+        # output-stage entry points cannot hide behind their agreement
+        o_ref, _ = oracle_heads(w, range(w.H), want_ht=False)
+        assert_o_close(got, o_ref, covered_tokens(w.cu_seqlens, w.T))
     # and the same problem twice more in a row on the shared static array
     w = cases[0]
     wd, h, vn, gc = _stage_inputs(w)
