@@ -305,3 +305,27 @@ def test_pipelined_host_forward_matches_device(parts):
                                               min_tokens=0)
     mask = torch.from_numpy(covered_tokens(w.cu_seqlens, w.T))
     assert torch.equal(o_h[mask], o_d.cpu()[mask]) and torch.equal(ht_h, ht_d.cpu())
+
+
+@pytest.mark.parametrize("path", ["fused", "staged"])
+def test_gate_rows_with_a_padded_token_stride(path):
+    # g and beta as views whose rows are H + 1 elements apart (the innermost stride is 1,
+    # as the boundary requires): the same values as contiguous tensors, so the outputs
+    # must be bit-identical, and they match the oracle
+    _skip_unsupported(path)
+    w = make_workload("gate_vec", 83, [300, 0, 77, 1], 2, 8, 64, with_h0=True)
+    wd = w.to("cuda")
+    kw = dict(scale=w.scale, initial_state=wd.h0, cu_seqlens=wd.cu_seqlens,
+              output_final_state=True, path=path)
+    o1, ht1 = api.chunk_fwd(wd.q, wd.k, wd.v, wd.g, wd.beta, **kw)
+    g2 = torch.zeros(w.T, w.H + 1, dtype=torch.float32, device="cuda")[:, :w.H]
+    b2 = torch.zeros(w.T, w.H + 1, dtype=torch.bfloat16, device="cuda")[:, :w.H]
+    g2.copy_(wd.g)
+    b2.copy_(wd.beta)
+    assert g2.stride(0) == w.H + 1 and b2.stride(0) == w.H + 1
+    o2, ht2 = api.chunk_fwd(wd.q, wd.k, wd.v, g2, b2, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(ht1, ht2)
+    o_ref, ht_ref = oracle_heads(w, range(w.H))
+    assert_o_close(o1, o_ref, covered_tokens(w.cu_seqlens, w.T))
+    assert_ht_close(ht1, ht_ref)
