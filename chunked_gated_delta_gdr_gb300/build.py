@@ -20,7 +20,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgdr.so")
 
 SOURCES = ["gdr_api.cu", "gdr_index.cu", "gdr_staged.cu", "gdr_fused.cu", "gdr_split.cu",
-           "gdr_bwd.cu"]
+           "gdr_bwd.cu", "gdr_bwd_tc.cu"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
               "--expt-relaxed-constexpr"]

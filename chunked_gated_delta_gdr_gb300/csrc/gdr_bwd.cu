@@ -774,10 +774,17 @@ cudaError_t launch_bwd_d(const BwdArgs &a, const BwdWs &w, cudaStream_t stream) 
                                Ckpt{nullptr, nullptr, 0}, a.seg, a.order, stream)) != cudaSuccess)
     return e;
   const dim3 gc((unsigned)s.chunk_cap, (unsigned)s.H);
-  if ((e = set_smem(k_bwd_dv_intra<D>, DvIntraSmem<D>::bytes)) != cudaSuccess) return e;
-  k_bwd_dv_intra<D><<<dim3(gc.x, gc.y, D / 64), kChunkThreads, DvIntraSmem<D>::bytes, stream>>>(
-      group, a.q, a.k, a.dout, vg, a.scale, vdvp, a.chunks, a.n_chunks, vec);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // dV' intra-chunk part on the tensor cores when TMA can load q, k and dout; the
+  // warp-tile kernel otherwise
+  e = launch_bwd_dv_intra_tc(a, vg, vdvp, stream);
+  if (e == cudaErrorNotSupported) {
+    (void)cudaGetLastError();
+    if ((e = set_smem(k_bwd_dv_intra<D>, DvIntraSmem<D>::bytes)) != cudaSuccess) return e;
+    k_bwd_dv_intra<D><<<dim3(gc.x, gc.y, D / 64), kChunkThreads, DvIntraSmem<D>::bytes, stream>>>(
+        group, a.q, a.k, a.dout, vg, a.scale, vdvp, a.chunks, a.n_chunks, vec);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) return e;
   auto scan = [&](auto kern, int cols, size_t bytes) -> cudaError_t {
     cudaError_t r = set_smem(kern, bytes);
     if (r != cudaSuccess) return r;
@@ -793,11 +800,18 @@ cudaError_t launch_bwd_d(const BwdArgs &a, const BwdWs &w, cudaStream_t stream) 
   e = bcols == 64 ? scan(k_bwd_scan<D, 64>, 64, BwdScanSmem<D, 64>::bytes)
                   : scan(k_bwd_scan<D, 32>, 32, BwdScanSmem<D, 32>::bytes);
   if (e != cudaSuccess) return e;
-  if ((e = set_smem(k_bwd_sgrad<D>, SgradSmem::bytes)) != cudaSuccess) return e;
-  k_bwd_sgrad<D><<<dim3(gc.x, gc.y, D / kSRows), kChunkThreads, SgradSmem::bytes, stream>>>(
-      a.dout, vn, vg, a.scale, reinterpret_cast<const __nv_bfloat16 *>(w.h), w.dh, vdvp, vdqh,
-      vdkh, vdw, w.sdot, a.chunks, a.n_chunks, s.H, vec);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // the S_0 / dS_C products on the tensor cores when TMA can load dout; the warp-tile
+  // kernel otherwise
+  e = launch_bwd_sgrad_tc(a, w.h, w.dh, vg, vn, vdvp, vdqh, vdkh, vdw, w.sdot, stream);
+  if (e == cudaErrorNotSupported) {
+    (void)cudaGetLastError();
+    if ((e = set_smem(k_bwd_sgrad<D>, SgradSmem::bytes)) != cudaSuccess) return e;
+    k_bwd_sgrad<D><<<dim3(gc.x, gc.y, D / kSRows), kChunkThreads, SgradSmem::bytes, stream>>>(
+        a.dout, vn, vg, a.scale, reinterpret_cast<const __nv_bfloat16 *>(w.h), w.dh, vdvp, vdqh,
+        vdkh, vdw, w.sdot, a.chunks, a.n_chunks, s.H, vec);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) return e;
   if ((e = set_smem(k_bwd_intra<D>, IntraSmem<D>::bytes)) != cudaSuccess) return e;
   k_bwd_intra<D><<<gc, kChunkThreads, IntraSmem<D>::bytes, stream>>>(group, a.q, a.k, a.dout, vn, vg,
                                                             a.scale, vdqh, vdkh, w.dga,

@@ -26,4 +26,17 @@ struct BwdArgs {
 size_t bwd_work_bytes(int64_t T, int32_t n_seq, int32_t Hk, int32_t H, int32_t D);
 cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t stream);
 
+// Tensor-core (tcgen05 / TMA) kernels of the backward (gdr_bwd_tc.cu).  Each returns
+// cudaErrorNotSupported, launching nothing, when its operands cannot be loaded by TMA
+// (base or strides not 16-byte aligned, head dim other than 64 or 128); the caller then
+// runs the warp-tile kernel of the same step.
+cudaError_t launch_bwd_dv_intra_tc(const BwdArgs &a, View gcum, View dvp, cudaStream_t stream);
+// The S_0 / dS_C products (dq, dk, dW parts and <dS_C, S_0> per 64 key rows) from the bf16
+// states h [chunks, H, D, D] and their fp32 gradients dh (same layout); dvp, dh also need
+// 16-byte aligned rows (float4 loads).
+cudaError_t launch_bwd_sgrad_tc(const BwdArgs &a, const void *h, const float *dh, View gcum,
+                               View vnew, View dvp, View dqh, View dkh, View dw, float *sdot,
+                               cudaStream_t stream);
+cudaError_t read_bwd_tc_status(int32_t *out);
+
 }  // namespace gdr

@@ -1206,6 +1206,11 @@ int g_num_sms[64] = {0};
 
 }  // namespace
 
+bool make_tile_map(CUtensorMap *m, const void *ptr, int64_t D, int64_t heads, int64_t T,
+                   int64_t st, int64_t sh) {
+  return make_map(m, ptr, D, heads, T, st, sh);
+}
+
 bool fused_supported(const FusedArgs &a) {
   if (a.D != 128 && a.D != 64) return false;
   auto al16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };

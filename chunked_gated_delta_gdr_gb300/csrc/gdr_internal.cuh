@@ -1,6 +1,7 @@
 // gdr_internal.cuh -- shared definitions of the libgdr CUDA sources (not installed).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -140,6 +141,11 @@ struct FusedArgs {
   void *workspace;  // fused-path scratch (work list etc.)
 };
 bool fused_supported(const FusedArgs &a);
+// TMA map of a [T, heads, D] bf16 tensor (element strides st, sh; innermost contiguous):
+// boxes of 64 tokens x 1 head x 64 elements, 128-byte swizzle (gdr_fused.cu).  False if the
+// driver's encoder rejects it (alignment of base or strides).
+bool make_tile_map(CUtensorMap *m, const void *ptr, int64_t D, int64_t heads, int64_t T,
+                   int64_t st, int64_t sh);
 size_t fused_workspace_bytes(int64_t T, int32_t n_seq, int32_t H);
 cudaError_t launch_fused(const FusedArgs &a, cudaStream_t stream);
 

@@ -85,7 +85,7 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
 // *abort becomes nonzero.  Returns true when the phase completed.  Waiting
 // threads are suspended between polls, so they do not take issue slots from
 // the warps doing the work.
-__device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity,
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity,
                                             const volatile int32_t *abort, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
@@ -250,6 +250,15 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int32_t c0, int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
       : "memory");
 }
 

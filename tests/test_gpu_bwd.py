@@ -155,8 +155,10 @@ def test_backward_full_size_packed_sampled_heads():
 
 def test_backward_unaligned_views_take_the_scalar_loads():
     # q, k, v and dout as views whose rows are not 16-byte aligned (an odd element
-    # offset into a larger buffer): the kernels fall back to element loads and must give
-    # the same gradients as the aligned call
+    # offset into a larger buffer): the kernels fall back to element loads, and the
+    # intra-chunk dV' step to its warp-tile kernel (the aligned call runs it on the tensor
+    # cores with P in bf16), so the gradients agree with the aligned call within the
+    # backward tolerance and with the oracle
     w = make_workload("unaligned", 61, [130, 0, 70], 1, 2, 64, with_h0=True)
     do, dht = _upstream(w, 62, True)
     ref = _run_bwd(w, do, dht)
@@ -174,7 +176,12 @@ def test_backward_unaligned_views_take_the_scalar_loads():
                         cu_seqlens=wd.cu_seqlens, dht=dht.cuda(), want_dh0=True)
     torch.cuda.synchronize()
     for name, a, b in zip(NAMES, got, ref):
-        assert torch.equal(a, b), name
+        scale = max(b.abs().max().item(), 1e-30)
+        assert (a - b).abs().max().item() <= REL * scale, name
+    ref64 = oracle.recurrent_bwd(w.q, w.k, w.v, w.g, w.beta, w.scale, w.h0, w.cu_seqlens, do, dht)
+    mask = covered_tokens(w.cu_seqlens, w.T)
+    for name, a, b in zip(NAMES, got, ref64):
+        _close(name, a, b, None if name == "dh0" else mask)
 
 
 def test_backward_only_empty_segments():
