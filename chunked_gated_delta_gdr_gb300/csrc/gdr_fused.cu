@@ -902,8 +902,14 @@ __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
         if constexpr (kVar == kVarSplit) {
           if (ui.mode == kUnitFull) state_from_h0(p, tmem_addr(tb + TM_S, lane_base, 0), sidx, dv);
           else state_from_split(p, tmem_addr(tb + TM_S, lane_base, 0), ui, dv);
-        } else {
+        } else if (p.has_h0) {
           state_from_h0(p, tmem_addr(tb + TM_S, lane_base, 0), sidx, dv);
+        } else {  // zero state, inline (the out-of-line call cost ~6000 cycles per unit)
+          uint32_t z[32];
+#pragma unroll
+          for (int u = 0; u < 32; ++u) z[u] = 0u;
+#pragma unroll 1
+          for (int cb = 0; cb < 4; ++cb) tmem_st32(tmem_addr(tb + TM_S, lane_base, cb * 32), z);
         }
       }
       if constexpr (kVar == kVarCkpt) {
