@@ -720,6 +720,7 @@ struct BwdWs {
   void *w, *u, *vnew;
   void *h;
   float *dvp, *dh, *dqh, *dkh, *dw, *dga, *sdot;
+  void *fws;  // the fused recompute's scratch (work list)
   size_t bytes;
 };
 
@@ -747,6 +748,7 @@ BwdWs carve_bwd(void *ws, int64_t T, int32_t n_seq, int32_t Hk, int32_t H, int32
   r.dw = reinterpret_cast<float *>(take(tok * D * sizeof(float)));
   r.dga = reinterpret_cast<float *>(take(tok * sizeof(float)));
   r.sdot = reinterpret_cast<float *>(take(cap * H * (D / kSRows) * sizeof(float)));
+  r.fws = take(fused_workspace_bytes(T, n_seq, H));
   r.bytes = off;
   return r;
 }
@@ -766,13 +768,57 @@ cudaError_t launch_bwd_d(const BwdArgs &a, const BwdWs &w, cudaStream_t stream) 
   };
   const bool vec = al(a.q) && al(a.k) && al(a.v) && al(a.dout);
   cudaError_t e;
-  // forward recompute: G, W, U (stage 1), chunk states h and V' (stage 2)
-  if ((e = launch_prep(s, a.k, a.v, a.g, a.beta, vw, vu, vg, a.seg, a.chunks, a.n_chunks,
-                       stream)) != cudaSuccess)
-    return e;
-  if ((e = launch_scan_ordered(s, a.k, vw, vu, vg, a.h0, w.h, vn, nullptr,
-                               Ckpt{nullptr, nullptr, 0}, a.seg, a.order, stream)) != cudaSuccess)
-    return e;
+  // forward recompute: G, W, the chunk states h and V', by the fused forward kernel's
+  // backward variant when TMA can load q, k and v; else by the staged stage 1 (G, W, U)
+  // and stage 2 (h, V')
+  FusedArgs fa{};
+  fa.T = s.T;
+  fa.n_seq = s.n_seq;
+  fa.Hk = s.Hk;
+  fa.H = s.H;
+  fa.D = D;
+  fa.q = a.q.p;
+  fa.k = a.k.p;
+  fa.v = a.v.p;
+  fa.q_st = a.q.st;
+  fa.q_sh = a.q.sh;
+  fa.k_st = a.k.st;
+  fa.k_sh = a.k.sh;
+  fa.v_st = a.v.st;
+  fa.v_sh = a.v.sh;
+  fa.g = reinterpret_cast<const float *>(a.g.p);
+  fa.g_st = a.g.st;
+  fa.g_sh = a.g.sh;
+  fa.beta = a.beta.p;
+  fa.b_st = a.beta.st;
+  fa.b_sh = a.beta.sh;
+  fa.scale = a.scale;
+  fa.h0 = a.h0;
+  fa.ckpt = Ckpt{nullptr, nullptr, 0};
+  fa.bwd.gcum = w.gcum;
+  fa.bwd.w = w.w;
+  fa.bwd.h = w.h;
+  fa.bwd.vnew = w.vnew;
+  fa.seg = a.seg;
+  fa.workspace = w.fws;
+  bool fused = fused_supported(fa);
+  if (fused) {
+    e = launch_fused(fa, stream);
+    if (e == cudaErrorInvalidValue) {  // a TMA map was refused: the staged recompute
+      (void)cudaGetLastError();
+      fused = false;
+    } else if (e != cudaSuccess) {
+      return e;
+    }
+  }
+  if (!fused) {
+    if ((e = launch_prep(s, a.k, a.v, a.g, a.beta, vw, vu, vg, a.seg, a.chunks, a.n_chunks,
+                         stream)) != cudaSuccess)
+      return e;
+    if ((e = launch_scan_ordered(s, a.k, vw, vu, vg, a.h0, w.h, vn, nullptr,
+                                 Ckpt{nullptr, nullptr, 0}, a.seg, a.order, stream)) != cudaSuccess)
+      return e;
+  }
   const dim3 gc((unsigned)s.chunk_cap, (unsigned)s.H);
   // dV' intra-chunk part on the tensor cores when TMA can load q, k and dout; the
   // warp-tile kernel otherwise

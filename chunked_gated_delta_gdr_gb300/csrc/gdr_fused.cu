@@ -82,8 +82,9 @@ struct UnitInfo {
   int32_t seq, head, t0, end, nch, mode, sin, sout;  // the last three: split units only
 };
 
-// kernel variants: the plain forward, with state checkpoints, split-segment pieces
-constexpr int kVarPlain = 0, kVarCkpt = 1, kVarSplit = 2;
+// kernel variants: the plain forward, with state checkpoints, split-segment pieces, and the
+// forward recomputed for the backward (no output; the chunk quantities the backward reads)
+constexpr int kVarPlain = 0, kVarCkpt = 1, kVarSplit = 2, kVarBwd = 3;
 
 // Per-chunk vectors, computed by the producer warp from g and beta.  Five slots
 // (by chunk index): the producer refills chunk c's slot for chunk c+5 only after
@@ -130,6 +131,10 @@ struct Params {
   int64_t o_st, o_sh;
   float *ht;
   Ckpt ckpt;                // state checkpoints (ckpt.h null: none)
+  // backward recompute (kVarBwd): G [T][H] fp32 (natural log), W and V' [T][H][D] bf16,
+  // the state entering each chunk [chunk][H][D dk][D dv] bf16
+  float *bw_gcum;
+  __nv_bfloat16 *bw_w, *bw_h, *bw_vn;
   SplitArgs split;          // split-segment pieces (split.units null: none)
   const SegInfo *seg;
   const int32_t *order;     // non-empty segments, longest first
@@ -319,6 +324,11 @@ __device__ void role_producer(const Params &p, Small *sm, uint8_t *base,
         cv.dec[j1] = ex2(GL - G1);
         cv.beta[j0] = b0;
         cv.beta[j1] = b1;
+        if constexpr (kVar == kVarBwd) {
+          float *gc = p.bw_gcum + (int64_t)t * p.H + ui.head;
+          if (j0 < len) gc[(int64_t)j0 * p.H] = sum - g1;
+          if (j1 < len) gc[(int64_t)j1 * p.H] = sum;
+        }
         if (lane == 0) {
           cv.eL = ex2(GL);
           cv.Gref = gmax;
@@ -366,6 +376,8 @@ __device__ void role_issue_p(const Params &p, Small *sm, uint8_t *base) {
   const uint64_t d_v = sdesc_sw128(sbase + OFF_STAGE + kKQBytes, 8192, 1024);  // V (MN-major)
   const uint64_t d_tb = sdesc_sw128(sbase + OFF_TB, 0, 1024);
   const uint64_t d_p = sdesc_sw128(sbase + OFF_P, 0, 1024);
+  const uint64_t d_kmn = sdesc_sw128(sbase + OFF_STAGE, 16384, 1024);  // K (MN-major)
+  const uint64_t d_tbg = sdesc_sw128(sbase + OFF_TBG, 0, 1024);
   uint32_t g = 0;
   bool ok = true;
   // X1 of chunk gg into its U buffer (by parity).  It needs its stage, prep done
@@ -418,6 +430,23 @@ __device__ void role_issue_p(const Params &p, Small *sm, uint8_t *base) {
           mma_bf16(tu, dadd(dv, kk * 2048), dadd(d_tb, kk * 32), id_uw, kk > 0);
       }
       mma_commit(&sm->uw_full);
+      if constexpr (kVar == kVarBwd) {
+        // no output: -W^T = K^T (-Tm diag(beta e^G))^T into the O accumulator instead, once
+        // the state warpgroup has read the previous chunk's and has started this chunk (its
+        // s_ready arrival follows its o1_full wait for the previous chunk: without it, at a
+        // unit boundary, this thread could commit o1_full twice ahead of that wait)
+        if (!wait1(sm, sm->s_ready, g & 1, 0x209)) { ok = false; break; }
+        if (g >= 1 && !wait1(sm, sm->o_free, (g - 1) & 1, 0x20a)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t dk = dadd(d_kmn, s * kStageBytes);
+#pragma unroll 1
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16(tb + TM_O, dadd(dk, kk * 2048), dadd(d_tbg, kk * 32), id_uw, kk > 0);
+        mma_commit(&sm->o1_full);
+        mma_commit(&sm->o_full);
+        mma_commit(&sm->empty[s]);
+        continue;
+      }
       // O^T (inter-chunk part) = S^T Q^T, once the epilogue has read the previous chunk's
       if (!wait1(sm, sm->s_ready, g & 1, 0x209)) { ok = false; break; }
       if (g >= 1 && !wait1(sm, sm->o_free, (g - 1) & 1, 0x20a)) { ok = false; break; }
@@ -549,6 +578,7 @@ __device__ __forceinline__ void warp_store16(float *C, int ldc, const float (&c)
 }
 
 // The prep warpgroup.  `row` is this thread's TMEM lane (0..127).
+template <bool kVarW>
 __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
   const uint32_t tb = sm->tmem_base;
   const uint32_t sbase = smem_u32(base);
@@ -725,6 +755,11 @@ __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
       {
         const int ri = pid & 63, hc = (pid >> 6) * 32;
         if (g >= 1 && !wait_wg(sm, sm->vp_full, (g - 1) & 1, 0x305, kBarPrep)) { ok = false; break; }
+        // (the backward recompute's W MMA reads Tm diag(beta e^G) too)
+        if (kVarW && g >= 1 && !wait_wg(sm, sm->o_full, (g - 1) & 1, 0x306, kBarPrep)) {
+          ok = false;
+          break;
+        }
         // 8 columns at a time: a rolled loop keeps this block small in the instruction
         // cache, which the SMs of a GPC share at full occupancy
 #pragma unroll 1
@@ -861,6 +896,28 @@ __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
     }
     return true;
   };
+  // backward recompute: W of chunk gg (-W^T, key dim on the lanes, in the O accumulator)
+  // to W[t][head][dk] bf16 for the chunk's tokens
+  auto w_out = [&](uint32_t gg) -> bool {
+    if (!wait_wg(sm, sm->o_full, gg & 1, 0x401, kBarState)) return false;
+    tc_fence_after();
+    uint32_t r0[32], r1[32];
+    tmem_ld32(tmem_addr(tb + TM_O, lane_base, 0), r0);
+    tmem_ld32(tmem_addr(tb + TM_O, lane_base, 32), r1);
+    tmem_ld_wait();
+    tc_fence_before();
+    mbar_arrive(&sm->o_free);
+    if (dv < D) {
+      const int64_t st = (int64_t)p.H * D;
+      __nv_bfloat16 *wp = p.bw_w + (int64_t)prev_t * st + (int64_t)prev_head * D + dv;
+#pragma unroll
+      for (int u = 0; u < 32; ++u) {
+        if (u < prev_len) wp[u * st] = __float2bfloat16_rn(-__uint_as_float(r0[u]));
+        if (32 + u < prev_len) wp[(32 + u) * st] = __float2bfloat16_rn(-__uint_as_float(r1[u]));
+      }
+    }
+    return true;
+  };
   // part 2: the staging tile to global memory, 16 bytes per store
   auto epi_store = [&]() {
     named_bar(kBarState, 128);
@@ -939,8 +996,34 @@ __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&sm->s_ready);
+      if constexpr (kVar == kVarBwd) {
+        // the state entering this chunk as the products use it (bf16) to h[chunk][dk][dv]:
+        // column m of the bf16 copy holds key dims 2m, 2m + 1 (rewritten only by this
+        // warpgroup's next state conversion)
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tmem_addr(tb + TM_SB, lane_base, 0), r0);
+        tmem_ld32(tmem_addr(tb + TM_SB, lane_base, 32), r1);
+        tmem_ld_wait();
+        if (dv < D) {
+          const int64_t cid = p.seg[ui.seq].chunk_off + c;
+          uint16_t *hp = reinterpret_cast<uint16_t *>(p.bw_h) + (cid * p.H + ui.head) * D * D + dv;
+#pragma unroll
+          for (int m = 0; m < 32; ++m) {
+            hp[(2 * m) * D] = (uint16_t)(r0[m] & 0xffffu);
+            hp[(2 * m + 1) * D] = (uint16_t)(r0[m] >> 16);
+          }
+          if (D == 128) {
+#pragma unroll
+            for (int m = 0; m < 32; ++m) {
+              hp[(64 + 2 * m) * D] = (uint16_t)(r1[m] & 0xffffu);
+              hp[(64 + 2 * m + 1) * D] = (uint16_t)(r1[m] >> 16);
+            }
+          }
+        }
+        if (c >= 1 && !w_out(g - 1)) { ok = false; break; }
+      }
       // previous chunk's output accumulators (same unit) -> staging, while Y is computed
-      if (c >= 1 && !epi_read(g - 1)) { ok = false; break; }
+      if (kVar != kVarBwd && c >= 1 && !epi_read(g - 1)) { ok = false; break; }
       // Y -> bf16 pairs in place; token columns past the chunk's end are zeroed so that
       // whatever the stage holds there cannot reach V'
       if (!wait_wg(sm, sm->y_full, g & 1, 0x405, kBarState)) { ok = false; break; }
@@ -963,7 +1046,7 @@ __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&sm->y_ready);
-      if (c >= 1) epi_store();
+      if (kVar != kVarBwd && c >= 1) epi_store();
       // V'^T -> bf16 V'^T (columns 0-31) and V''^T = V'^T diag(e^{G_last - G}) (32-63)
       if (!wait_wg(sm, sm->vp_full, g & 1, 0x406, kBarState)) { ok = false; break; }
       tc_fence_after();
@@ -975,6 +1058,19 @@ __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
         tmem_ld_wait();
         pack64(r0, r1, pk);
         tmem_st32(tmem_addr(tu, lane_base, 0), pk);
+        if constexpr (kVar == kVarBwd) {
+          // V' (bf16, as the products use it) to V'[t][head][dv]; pk[m] holds tokens 2m, 2m + 1
+          if (dv < D) {
+            const int64_t st = (int64_t)p.H * D;
+            uint16_t *vp = reinterpret_cast<uint16_t *>(p.bw_vn) + (int64_t)t * st +
+                           (int64_t)ui.head * D + dv;
+#pragma unroll
+            for (int m = 0; m < 32; ++m) {
+              if (2 * m < len) vp[(2 * m) * st] = (uint16_t)(pk[m] & 0xffffu);
+              if (2 * m + 1 < len) vp[(2 * m + 1) * st] = (uint16_t)(pk[m] >> 16);
+            }
+          }
+        }
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           float d[4];
@@ -1027,8 +1123,12 @@ __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
                     D, dv);
       }
     }
-    if (!epi_read(g - 1)) break;
-    epi_store();
+    if constexpr (kVar == kVarBwd) {
+      if (!w_out(g - 1)) break;
+    } else {
+      if (!epi_read(g - 1)) break;
+      epi_store();
+    }
   }
 }
 
@@ -1100,7 +1200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 2) {
     if (lane == 0) role_issue_c<kVar>(p, sm, base);
   } else if (warp < 7) {
-    role_prep(p, sm, base, 32 * (warp & 3) + lane);
+    role_prep<kVar == kVarBwd>(p, sm, base, 32 * (warp & 3) + lane);
   } else {
     role_state<kVar>(p, sm, base, 32 * (warp & 3) + lane);
   }
@@ -1266,6 +1366,8 @@ cudaError_t launch_fused(const FusedArgs &a, cudaStream_t stream) {
         (e = cudaFuncSetAttribute(k_fused<kVarCkpt>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)kSmemBytes)) != cudaSuccess ||
         (e = cudaFuncSetAttribute(k_fused<kVarSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)kSmemBytes)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(k_fused<kVarBwd>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)kSmemBytes)) != cudaSuccess)
       return e;
     g_num_sms[dev] = n;
@@ -1290,6 +1392,10 @@ cudaError_t launch_fused(const FusedArgs &a, cudaStream_t stream) {
   p.o_sh = a.o_sh;
   p.ht = a.ht;
   p.ckpt = a.ckpt;
+  p.bw_gcum = a.bwd.gcum;
+  p.bw_w = reinterpret_cast<__nv_bfloat16 *>(a.bwd.w);
+  p.bw_h = reinterpret_cast<__nv_bfloat16 *>(a.bwd.h);
+  p.bw_vn = reinterpret_cast<__nv_bfloat16 *>(a.bwd.vnew);
   p.split = a.split;
   p.seg = a.seg;
   p.order = order;
@@ -1304,6 +1410,8 @@ cudaError_t launch_fused(const FusedArgs &a, cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
   if (split)
     k_fused<kVarSplit><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+  else if (p.bw_h)
+    k_fused<kVarBwd><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
   else if (p.ckpt.h)
     k_fused<kVarCkpt><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
   else

@@ -137,6 +137,13 @@ struct FusedArgs {
   float *ht;
   Ckpt ckpt;
   SplitArgs split;
+  // The forward recomputed for the backward instead (bwd.h non-null; no o, no ht): the
+  // chunk-local cumulative gate G [T][H] fp32, W = Tm diag(beta e^G) K and V' [T][H][D]
+  // bf16, and the state entering each chunk [chunk][H][D][D] bf16 (chunk ids of `seg`)
+  struct {
+    float *gcum;
+    void *w, *h, *vnew;
+  } bwd;
   const SegInfo *seg;
   void *workspace;  // fused-path scratch (work list etc.)
 };
