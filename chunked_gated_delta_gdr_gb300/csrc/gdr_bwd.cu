@@ -466,8 +466,8 @@ struct WySmem {
 template <int D>
 __global__ void __launch_bounds__(kChunkThreads, 2)
     k_bwd_wy(int32_t group, View k, View v, View beta, View gcum, View dvp, View dw, View dkh,
-             const float *dga, const float *sdot, View dv_out, View dbeta_out, View dg_out,
-             const ChunkInfo *__restrict__ chunks, const int32_t *__restrict__ n_chunks,
+             const float *dga, const float *sdot, const float *tg, View dv_out, View dbeta_out,
+             View dg_out, const ChunkInfo *__restrict__ chunks, const int32_t *__restrict__ n_chunks,
              int32_t H, bool vec) {
   extern __shared__ float sm[];
   constexpr int LB = WySmem::kLdB, LF = WySmem::kLdF, LT = WySmem::kLdT;
@@ -532,7 +532,20 @@ __global__ void __launch_bounds__(kChunkThreads, 2)
       dT[i * LT + j] = lo ? B[j] * du[b][e] + BG[j] * dwk[b][e] : 0.f;
     }
   __syncthreads();  // also: every warp is done with the pass tiles (the solve's scratch)
-  solve_unit_lower64(X, LT, Tm, LT, scratch, kChunkThreads, 0);  // T = (I + A)^-1
+  if (tg) {  // T = (I + A)^-1 as the fused recompute formed it
+    const float *tc = tg + ((int64_t)cid * H + h) * 4096;
+    for (int idx = tid; idx < 64 * 16; idx += kChunkThreads) {
+      const int i = idx >> 4, j = (idx & 15) * 4;
+      const float4 x = *reinterpret_cast<const float4 *>(tc + i * 64 + j);
+      Tm[i * LT + j] = x.x;
+      Tm[i * LT + j + 1] = x.y;
+      Tm[i * LT + j + 2] = x.z;
+      Tm[i * LT + j + 3] = x.w;
+    }
+    __syncthreads();
+  } else {
+    solve_unit_lower64(X, LT, Tm, LT, scratch, kChunkThreads, 0);  // T = (I + A)^-1
+  }
   // X = dT T^T
   {
     float accs[kTPW][4] = {};
@@ -720,7 +733,8 @@ struct BwdWs {
   void *w, *u, *vnew;
   void *h;
   float *dvp, *dh, *dqh, *dkh, *dw, *dga, *sdot;
-  void *fws;  // the fused recompute's scratch (work list)
+  void *fws;    // the fused recompute's scratch (work list)
+  float *tmat;  // Tm per chunk and head from the fused recompute [chunk][H][64][64]
   size_t bytes;
 };
 
@@ -749,6 +763,7 @@ BwdWs carve_bwd(void *ws, int64_t T, int32_t n_seq, int32_t Hk, int32_t H, int32
   r.dga = reinterpret_cast<float *>(take(tok * sizeof(float)));
   r.sdot = reinterpret_cast<float *>(take(cap * H * (D / kSRows) * sizeof(float)));
   r.fws = take(fused_workspace_bytes(T, n_seq, H));
+  r.tmat = reinterpret_cast<float *>(take(cap * H * 64 * 64 * sizeof(float)));
   r.bytes = off;
   return r;
 }
@@ -799,6 +814,7 @@ cudaError_t launch_bwd_d(const BwdArgs &a, const BwdWs &w, cudaStream_t stream) 
   fa.bwd.w = w.w;
   fa.bwd.h = w.h;
   fa.bwd.vnew = w.vnew;
+  fa.bwd.tmat = w.tmat;
   fa.seg = a.seg;
   fa.workspace = w.fws;
   bool fused = fused_supported(fa);
@@ -865,7 +881,8 @@ cudaError_t launch_bwd_d(const BwdArgs &a, const BwdWs &w, cudaStream_t stream) 
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = set_smem(k_bwd_wy<D>, WySmem::bytes)) != cudaSuccess) return e;
   k_bwd_wy<D><<<gc, kChunkThreads, WySmem::bytes, stream>>>(group, a.k, a.v, a.beta, vg, vdvp, vdw,
-                                                      vdkh, w.dga, w.sdot, a.dv, a.dbeta, a.dg,
+                                                      vdkh, w.dga, w.sdot, fused ? w.tmat : nullptr,
+                                                      a.dv, a.dbeta, a.dg,
                                                       a.chunks, a.n_chunks, s.H, vec);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (group > 1) {

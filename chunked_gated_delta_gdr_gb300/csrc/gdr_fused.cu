@@ -135,6 +135,7 @@ struct Params {
   // the state entering each chunk [chunk][H][D dk][D dv] bf16
   float *bw_gcum;
   __nv_bfloat16 *bw_w, *bw_h, *bw_vn;
+  float *bw_t;  // Tm = (I + A)^-1 per chunk [chunk][H][64][64] fp32 (null: not stored)
   SplitArgs split;          // split-segment pieces (split.units null: none)
   const SegInfo *seg;
   const int32_t *order;     // non-empty segments, longest first
@@ -750,6 +751,21 @@ __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
         warp_store16(AS + (32 + 16 * mt) * kLdA + 16 * nt, kLdA, acc2, -1.f);
       }
       named_bar(kBarPrep, 128);
+      if (kVarW && p.bw_t) {
+        // Tm itself for the backward (fp32), half a row per thread; the scratch holds only
+        // its lower triangle and diagonal
+        const int ri = pid & 63, hc = (pid >> 6) * 32;
+        const int64_t cid = p.seg[ui.seq].chunk_off + c;
+        float *tg = p.bw_t + ((cid * p.H + ui.head) * 64 + ri) * 64 + hc;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float v4[4];
+          ld_f4(AS + ri * kLdA + hc + q * 4, v4);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) v4[u] = hc + q * 4 + u <= ri ? v4[u] : 0.f;
+          st_f4(tg + q * 4, v4);
+        }
+      }
       // Tm diag(beta) and -Tm diag(beta e^G) as bf16 operands, half a row per thread,
       // once the previous chunk's MMAs that read them are done
       {
@@ -1396,6 +1412,7 @@ cudaError_t launch_fused(const FusedArgs &a, cudaStream_t stream) {
   p.bw_w = reinterpret_cast<__nv_bfloat16 *>(a.bwd.w);
   p.bw_h = reinterpret_cast<__nv_bfloat16 *>(a.bwd.h);
   p.bw_vn = reinterpret_cast<__nv_bfloat16 *>(a.bwd.vnew);
+  p.bw_t = a.bwd.tmat;
   p.split = a.split;
   p.seg = a.seg;
   p.order = order;

@@ -139,10 +139,12 @@ struct FusedArgs {
   SplitArgs split;
   // The forward recomputed for the backward instead (bwd.h non-null; no o, no ht): the
   // chunk-local cumulative gate G [T][H] fp32, W = Tm diag(beta e^G) K and V' [T][H][D]
-  // bf16, and the state entering each chunk [chunk][H][D][D] bf16 (chunk ids of `seg`)
+  // bf16, the state entering each chunk [chunk][H][D][D] bf16 (chunk ids of `seg`), and
+  // Tm = (I + A)^-1 [chunk][H][64][64] fp32 (tmat may be null)
   struct {
     float *gcum;
     void *w, *h, *vnew;
+    float *tmat;
   } bwd;
   const SegInfo *seg;
   void *workspace;  // fused-path scratch (work list etc.)
