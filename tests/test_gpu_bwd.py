@@ -153,6 +153,23 @@ def test_backward_full_size_packed_sampled_heads():
     _close("dh0", got[5][:, hv], ref[5])
 
 
+def test_backward_many_units_per_block():
+    # more (segment, head) units than the GPU has SMs, so that every block of the fused
+    # recompute crosses unit boundaries (where a unit's last W is read at the end of the
+    # unit): no bounded wait may run out, and the gradients match the oracle
+    rng = np.random.default_rng(7)
+    lens = [int(x) for x in rng.integers(1, 260, size=160)] + [0, 0]
+    w = make_workload("many_units", 81, lens, 1, 2, 64, with_h0=True)
+    do, dht = _upstream(w, 82, True)
+    api.clear_device_status()
+    got = _run_bwd(w, do, dht)
+    assert api.device_status() == 0
+    ref = oracle.recurrent_bwd(w.q, w.k, w.v, w.g, w.beta, w.scale, w.h0, w.cu_seqlens, do, dht)
+    mask = covered_tokens(w.cu_seqlens, w.T)
+    for name, a, b in zip(NAMES, got, ref):
+        _close(name, a, b, None if name == "dh0" else mask)
+
+
 def test_backward_unaligned_views_take_the_scalar_loads():
     # q, k, v and dout as views whose rows are not 16-byte aligned (an odd element
     # offset into a larger buffer): the kernels fall back to element loads, and the
