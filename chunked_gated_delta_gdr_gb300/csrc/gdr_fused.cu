@@ -197,6 +197,30 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                "r"(d));
 }
 
+// Two fp32 products, or two fused multiply-adds, in one packed instruction (sm_100 and
+// later).  Each lane rounds exactly as the scalar operation does (round to nearest, no
+// flush to zero), so the results are those of the scalar code with half the instructions.
+// a, b: fp32 bit patterns (TMEM loads), times x, y.
+__device__ __forceinline__ void mul_x2(uint32_t &a, uint32_t &b, float x, float y) {
+  asm("{\n\t.reg .b64 s, t;\n\tmov.b64 s, {%0, %1};\n\tmov.b64 t, {%2, %3};\n\t"
+      "mul.rn.f32x2 s, s, t;\n\tmov.b64 {%0, %1}, s;\n\t}"
+      : "+r"(a), "+r"(b)
+      : "f"(x), "f"(y));
+}
+__device__ __forceinline__ void mul_x2(float &a, float &b, float x, float y) {
+  asm("{\n\t.reg .b64 s, t;\n\tmov.b64 s, {%0, %1};\n\tmov.b64 t, {%2, %3};\n\t"
+      "mul.rn.f32x2 s, s, t;\n\tmov.b64 {%0, %1}, s;\n\t}"
+      : "+f"(a), "+f"(b)
+      : "f"(x), "f"(y));
+}
+// (a, b) = (x a + u, y b + v)
+__device__ __forceinline__ void fma_x2(float &a, float &b, float x, float y, float u, float v) {
+  asm("{\n\t.reg .b64 s, t, c;\n\tmov.b64 s, {%0, %1};\n\tmov.b64 t, {%2, %3};\n\t"
+      "mov.b64 c, {%4, %5};\n\tfma.rn.f32x2 s, s, t, c;\n\tmov.b64 {%0, %1}, s;\n\t}"
+      : "+f"(a), "+f"(b)
+      : "f"(x), "f"(y), "f"(u), "f"(v));
+}
+
 __device__ __forceinline__ void zero_row(uint32_t tile, int row) {
 #pragma unroll
   for (int q = 0; q < 8; ++q) st_shared_v4(tile + row * 128 + q * 16, 0u, 0u, 0u, 0u);
@@ -671,9 +695,12 @@ __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
           }
           tmem_ld_wait();
 #pragma unroll
-          for (int u = 0; u < 32; ++u) {
-            const float prod = (ci * f[u]) * __uint_as_float(r[u]);
-            f[u] = u <= lim ? prod : 0.f;
+          for (int u = 0; u < 32; u += 2) {
+            float p0 = f[u], p1 = f[u + 1];
+            mul_x2(p0, p1, ci, ci);
+            mul_x2(p0, p1, __uint_as_float(r[u]), __uint_as_float(r[u + 1]));
+            f[u] = u <= lim ? p0 : 0.f;
+            f[u + 1] = u + 1 <= lim ? p1 : 0.f;
           }
           if (is_a) {
 #pragma unroll
@@ -789,10 +816,14 @@ __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
           ld_f4(cv.eG + c0, e8);
           ld_f4(cv.eG + c0 + 4, e8 + 4);
 #pragma unroll
-          for (int u = 0; u < 8; ++u) v[u] = (c0 + u <= ri) ? t8[u] * b8[u] : 0.f;
+          for (int u = 0; u < 8; u += 2) {
+            mul_x2(t8[u], t8[u + 1], b8[u], b8[u + 1]);
+            v[u] = (c0 + u <= ri) ? t8[u] : 0.f;
+            v[u + 1] = (c0 + u + 1 <= ri) ? t8[u + 1] : 0.f;
+          }
           store_chunk8(sbase + OFF_TB, ri, c0, v);
 #pragma unroll
-          for (int u = 0; u < 8; ++u) v[u] *= -e8[u];
+          for (int u = 0; u < 8; u += 2) mul_x2(v[u], v[u + 1], -e8[u], -e8[u + 1]);
           store_chunk8(sbase + OFF_TBG, ri, c0, v);
         }
       }
@@ -906,9 +937,12 @@ __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
         mbar_arrive(&sm->o_free);
       }
 #pragma unroll
-      for (int u = 0; u < 32; ++u)
-        st[(hb * 32 + u) * 128] =
-            __float2bfloat16_rn(fmaf(e[u], __uint_as_float(r1[u]), __uint_as_float(r2[u])));
+      for (int u = 0; u < 32; u += 2) {
+        float o0 = __uint_as_float(r1[u]), o1 = __uint_as_float(r1[u + 1]);
+        fma_x2(o0, o1, e[u], e[u + 1], __uint_as_float(r2[u]), __uint_as_float(r2[u + 1]));
+        st[(hb * 32 + u) * 128] = __float2bfloat16_rn(o0);
+        st[(hb * 32 + u + 1) * 128] = __float2bfloat16_rn(o1);
+      }
     }
     return true;
   };
@@ -1002,9 +1036,9 @@ __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
         pack64(r0, r1, pk);
         tmem_st32(tmem_addr(tb + TM_SB, lane_base, hb * 32), pk);
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          r0[u] = __float_as_uint(__uint_as_float(r0[u]) * eL);
-          r1[u] = __float_as_uint(__uint_as_float(r1[u]) * eL);
+        for (int u = 0; u < 32; u += 2) {
+          mul_x2(r0[u], r0[u + 1], eL, eL);
+          mul_x2(r1[u], r1[u + 1], eL, eL);
         }
         tmem_st32(tmem_addr(tb + TM_S, lane_base, hb * 64), r0);
         tmem_st32(tmem_addr(tb + TM_S, lane_base, hb * 64 + 32), r1);
@@ -1092,10 +1126,10 @@ __device__ void role_state(const Params &p, Small *sm, uint8_t *base, int row) {
           float d[4];
           ld_f4(cv.dec + q * 4, d);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) r0[q * 4 + u] = __float_as_uint(__uint_as_float(r0[q * 4 + u]) * d[u]);
+          for (int u = 0; u < 4; u += 2) mul_x2(r0[q * 4 + u], r0[q * 4 + u + 1], d[u], d[u + 1]);
           ld_f4(cv.dec + 32 + q * 4, d);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) r1[q * 4 + u] = __float_as_uint(__uint_as_float(r1[q * 4 + u]) * d[u]);
+          for (int u = 0; u < 4; u += 2) mul_x2(r1[q * 4 + u], r1[q * 4 + u + 1], d[u], d[u + 1]);
         }
         pack64(r0, r1, pk);
         tmem_st32(tmem_addr(tu, lane_base, 32), pk);
