@@ -564,24 +564,23 @@ __device__ __forceinline__ void st_f4(float *p, const float *v) {
   *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
 }
 
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
-
 // One warp: c[16 x 16] += A[16 x K] * B[K x 16] on the tensor pipe (tf32 in, fp32
-// accumulate, mma.sync m16n8k8); A and B are fp32 row-major in shared memory.
+// accumulate, mma.sync m16n8k8); A and B are fp32 row-major in shared memory.  The fp32
+// bit patterns go to the tensor core as they are: it reads the sign, exponent and top 10
+// mantissa bits of each tf32 operand, i.e. the operands are truncated to tf32 (relative
+// error below 2^-10) instead of rounded by a conversion instruction per element.
 __device__ __forceinline__ void warp_mm16(const float *A, int lda, const float *B, int ldb,
                                           int K, float (&c)[2][4]) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   for (int k = 0; k < K; k += 8) {
-    const uint32_t a0 = to_tf32(A[g * lda + k + t]), a1 = to_tf32(A[(g + 8) * lda + k + t]);
-    const uint32_t a2 = to_tf32(A[g * lda + k + t + 4]), a3 = to_tf32(A[(g + 8) * lda + k + t + 4]);
+    const uint32_t a0 = __float_as_uint(A[g * lda + k + t]);
+    const uint32_t a1 = __float_as_uint(A[(g + 8) * lda + k + t]);
+    const uint32_t a2 = __float_as_uint(A[g * lda + k + t + 4]);
+    const uint32_t a3 = __float_as_uint(A[(g + 8) * lda + k + t + 4]);
 #pragma unroll
     for (int n = 0; n < 2; ++n) {
-      const uint32_t b0 = to_tf32(B[(k + t) * ldb + n * 8 + g]);
-      const uint32_t b1 = to_tf32(B[(k + t + 4) * ldb + n * 8 + g]);
+      const uint32_t b0 = __float_as_uint(B[(k + t) * ldb + n * 8 + g]);
+      const uint32_t b1 = __float_as_uint(B[(k + t + 4) * ldb + n * 8 + g]);
       asm volatile(
           "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
           "{%8,%9}, {%0,%1,%2,%3};"
