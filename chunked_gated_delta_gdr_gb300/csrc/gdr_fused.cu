@@ -611,6 +611,10 @@ __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
   float *YS = reinterpret_cast<float *>(base + OFF_Y);  // 32 x kLdY fp32 (also 2 x 16 x kLdX)
   const int pid = row;           // 0..127, unique in the warpgroup
   const int wq = pid >> 5;       // warp index by lane quadrant
+  // the operand tiles Tm diag(beta) and -Tm diag(beta e^G) are zero above the diagonal's
+  // 8-column groups: cleared once here, only the lower groups are rewritten per chunk
+  for (int i = pid; i < 16384 / 16; i += 128) st_shared_v4(sbase + OFF_TB + i * 16, 0u, 0u, 0u, 0u);
+  fence_async_smem();
   uint32_t g = 0;
   bool ok = true;
   for (uint32_t k = 0; ok; ++k) {
@@ -693,13 +697,21 @@ __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
             for (int u = 0; u < 32; ++u) f[u] = ex2(gi - f[u]);
           }
           tmem_ld_wait();
+          if ((hh == 0) != upper) {  // the whole half is below the diagonal: nothing to mask
 #pragma unroll
-          for (int u = 0; u < 32; u += 2) {
-            float p0 = f[u], p1 = f[u + 1];
-            mul_x2(p0, p1, ci, ci);
-            mul_x2(p0, p1, __uint_as_float(r[u]), __uint_as_float(r[u + 1]));
-            f[u] = u <= lim ? p0 : 0.f;
-            f[u + 1] = u + 1 <= lim ? p1 : 0.f;
+            for (int u = 0; u < 32; u += 2) {
+              mul_x2(f[u], f[u + 1], ci, ci);
+              mul_x2(f[u], f[u + 1], __uint_as_float(r[u]), __uint_as_float(r[u + 1]));
+            }
+          } else {
+#pragma unroll
+            for (int u = 0; u < 32; u += 2) {
+              float p0 = f[u], p1 = f[u + 1];
+              mul_x2(p0, p1, ci, ci);
+              mul_x2(p0, p1, __uint_as_float(r[u]), __uint_as_float(r[u + 1]));
+              f[u] = u <= lim ? p0 : 0.f;
+              f[u + 1] = u + 1 <= lim ? p1 : 0.f;
+            }
           }
           if (is_a) {
 #pragma unroll
@@ -792,21 +804,25 @@ __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
           st_f4(tg + q * 4, v4);
         }
       }
-      // Tm diag(beta) and -Tm diag(beta e^G) as bf16 operands, half a row per thread,
-      // once the previous chunk's MMAs that read them are done
+      // Tm diag(beta) and -Tm diag(beta e^G) as bf16 operands, once the previous chunk's
+      // MMAs that read them are done
       {
-        const int ri = pid & 63, hc = (pid >> 6) * 32;
         if (g >= 1 && !wait_wg(sm, sm->vp_full, (g - 1) & 1, 0x305, kBarPrep)) { ok = false; break; }
         // (the backward recompute's W MMA reads Tm diag(beta e^G) too)
         if (kVarW && g >= 1 && !wait_wg(sm, sm->o_full, (g - 1) & 1, 0x306, kBarPrep)) {
           ok = false;
           break;
         }
-        // 8 columns at a time: a rolled loop keeps this block small in the instruction
-        // cache, which the SMs of a GPC share at full occupancy
+        // 8 columns at a time, lower-triangle groups only: row r holds r/8 + 1 of them, so
+        // rows q and 63 - q together hold 9, which the pair's four threads share (at most
+        // three each).  A rolled loop keeps this block small in the instruction cache,
+        // which the SMs of a GPC share at full occupancy.
+        const int q = pid >> 2, nq = (q >> 3) + 1;
 #pragma unroll 1
-        for (int q8 = 0; q8 < 32; q8 += 8) {
-          const int c0 = hc + q8;
+        for (int gi = pid & 3; gi < 9; gi += 4) {
+          const int ri = gi < nq ? q : 63 - q;
+          const int c0 = 8 * (gi < nq ? gi : gi - nq);
+          const int lim = ri - c0;  // column c0 + u is on or below the diagonal for u <= lim
           float t8[8], b8[8], e8[8], v[8];
           ld_f4(AS + ri * kLdA + c0, t8);
           ld_f4(AS + ri * kLdA + c0 + 4, t8 + 4);
@@ -817,8 +833,8 @@ __device__ void role_prep(const Params &p, Small *sm, uint8_t *base, int row) {
 #pragma unroll
           for (int u = 0; u < 8; u += 2) {
             mul_x2(t8[u], t8[u + 1], b8[u], b8[u + 1]);
-            v[u] = (c0 + u <= ri) ? t8[u] : 0.f;
-            v[u + 1] = (c0 + u + 1 <= ri) ? t8[u + 1] : 0.f;
+            v[u] = (u <= lim) ? t8[u] : 0.f;
+            v[u + 1] = (u + 1 <= lim) ? t8[u + 1] : 0.f;
           }
           store_chunk8(sbase + OFF_TB, ri, c0, v);
 #pragma unroll
